@@ -1,0 +1,505 @@
+"""Benchmark of the block-quantized wire codec on GB300.
+
+One step is one pass of the whole codec path over the prefill-scale workload:
+
+    4 x BF16 [65536, 7168]  --quant_i8-->  4 INT8 wires
+    4 wires                 --dequant_accum_i8 (W=4, FP32, source order)-->  1 wire
+    that wire               --dequant_i8-->  BF16 [65536, 7168]
+    wire 0 + BF16 buffer 1  --ring_hop_i8-->  1 wire
+    6 x BF16 [4096, 7168]   --quant_mx (staged slices)-->  MXFP8 [4096, 43008]
+    MXFP8 [4096, 43008]     --dequant_mx-->  BF16 [4096, 43008]
+
+(14 kernel launches). ``value`` is the step's algorithmic bytes (every input byte
+read once, every output byte written once) divided by the device time of the step,
+summed over ranks. The step's working set (about 12.5 GB) is far larger than the
+129 MB L2, so no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bq|reference]
+
+Under torchrun every rank runs its own replica of the workload on its own GPU (the
+path shards into independent blocks; there is no exchange step), with a barrier and
+the maximum over ranks of the timed region. ``--impl reference`` times the CPU oracle
+on a bounded sample of the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "codec HBM GB/s (and % of ~8 TB/s peak) per kernel at 1 GB300; bit-exact vs oracle"
+UNIT = "GB/s"
+HIDDEN = 7168
+W_SRC = 4
+N_SLICES = 6
+BF16 = 2
+
+
+def wire_per_value() -> float:
+    return 132.0 / 128.0
+
+
+def kernel_bytes(name: str, n: int) -> int:
+    """Algorithmic bytes of one launch over n values (inputs read once, outputs written once)."""
+    w = wire_per_value()
+    per = {
+        "quant_i8": BF16 + w,
+        "dequant_i8": w + BF16,
+        "dequant_accum_i8": W_SRC * w + w,
+        "ring_hop_i8": w + BF16 + w,
+        "quant_mx": BF16 + w,
+        "dequant_mx": w + BF16,
+    }[name]
+    return int(round(per * n))
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (timing aggregation only; not part of the data path)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- measurement helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary (profiles/ncu_traffic.txt):
+    lines 'kernel source_sha256 workload_values dram_bytes_per_launch_at_full_size'."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        line = line.split("#", 1)[0].split()
+        if len(line) >= 3:
+            out[line[0]] = (line[1], float(line[2]))
+    return out
+
+
+def kernel_sources_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_wire_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms; only samples taken
+    between mark_start() and mark_stop() (the timed region) are summarized."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def mark_start(self):
+        import datetime
+        self.t0 = datetime.datetime.now()
+
+    def mark_stop(self):
+        import datetime
+        self.t1 = datetime.datetime.now()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        import datetime
+        sms, maxs, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            if self.t0 is not None and not (self.t0 <= ts <= self.t1):
+                continue
+            sms.append(sm)
+            maxs.append(mx)
+            try:
+                power.append(float(parts[3]))
+            except ValueError:
+                pass
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- the workload
+class Pipeline:
+    """Device buffers and launch list of one codec step (caller-owned memory)."""
+
+    def __init__(self, rows: int, slice_rows: int, device):
+        from block_quantized_wire_gb300 import codec, inputs
+        self.codec = codec
+        self.rows, self.slice_rows = rows, slice_rows
+        self.n = rows * HIDDEN
+        self.n_slice = slice_rows * HIDDEN
+        self.xs = [inputs.prefill_buffer(w, device=device, rows=rows) for w in range(W_SRC)]
+        self.slices = inputs.mx_slices_4096(device=device, rows=slice_rows)
+        self.wires = [codec.empty_wire_i8(self.n, device) for _ in range(W_SRC)]
+        self.acc = codec.empty_wire_i8(self.n, device)
+        self.hop = codec.empty_wire_i8(self.n, device)
+        self.out = torch.empty((rows, HIDDEN), dtype=torch.bfloat16, device=device)
+        C = HIDDEN * N_SLICES
+        self.mx_q, self.mx_s = codec.empty_mx(slice_rows, C, device)
+        self.mx_out = torch.empty((slice_rows, C), dtype=torch.bfloat16, device=device)
+        self.launches = self._launch_list()
+
+    def _launch_list(self):
+        c = self.codec
+        L = []
+        for w in range(W_SRC):
+            L.append(("quant_i8", (lambda w=w: c.quant_i8(self.xs[w].view(-1), self.wires[w][1], self.wires[w][2])),
+                      kernel_bytes("quant_i8", self.n)))
+        L.append(("dequant_accum_i8", lambda: c.dequant_accum_i8(
+            [w[1] for w in self.wires], [w[2] for w in self.wires], self.acc[1], self.acc[2], None),
+            kernel_bytes("dequant_accum_i8", self.n)))
+        L.append(("dequant_i8", lambda: c.dequant_i8(self.acc[1], self.acc[2], self.out.view(-1)),
+                  kernel_bytes("dequant_i8", self.n)))
+        L.append(("ring_hop_i8", lambda: c.ring_hop_i8(self.wires[0][1], self.wires[0][2], self.xs[1].view(-1),
+                                                       self.hop[1], self.hop[2], None),
+                  kernel_bytes("ring_hop_i8", self.n)))
+        for i in range(N_SLICES):
+            c0 = i * HIDDEN
+            L.append(("quant_mx", (lambda i=i, c0=c0: c.quant_mx(
+                self.slices[i], self.mx_q[:, c0:c0 + HIDDEN], self.mx_s[:, c0 // 32:(c0 + HIDDEN) // 32])),
+                kernel_bytes("quant_mx", self.n_slice)))
+        L.append(("dequant_mx", lambda: c.dequant_mx(self.mx_q, self.mx_s, self.mx_out),
+                  kernel_bytes("dequant_mx", self.n_slice * N_SLICES)))
+        return L
+
+    def step_bytes(self) -> int:
+        return sum(b for _, _, b in self.launches)
+
+    def run(self, events=None):
+        for i, (_, fn, _) in enumerate(self.launches):
+            fn()
+            if events is not None:
+                events[i].record()
+
+    # end-to-end: host inputs in, host results out
+    def host_buffers(self):
+        pin = dict(pin_memory=True)
+        self.h_xs = [torch.empty_like(x, device="cpu", **pin).copy_(x) for x in self.xs]
+        self.h_slices = [torch.empty_like(x, device="cpu", **pin).copy_(x) for x in self.slices]
+        self.h_results = [torch.empty_like(t, device="cpu", **pin) for t in self.results()]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_xs + self.h_slices)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_results)
+
+    def results(self):
+        return [self.acc[0], self.out, self.hop[0], self.mx_q, self.mx_s, self.mx_out]
+
+    def run_e2e(self):
+        for d, h in zip(self.xs, self.h_xs):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(self.slices, self.h_slices):
+            d.copy_(h, non_blocking=True)
+        self.run()
+        for h, d in zip(self.h_results, self.results()):
+            h.copy_(d, non_blocking=True)
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample(pipe_inputs, rows: int, slice_rows: int):
+    """Run the oracle over the first `rows` rows of every prefill buffer and the first
+    `slice_rows` rows of every MX slice, in the step's order. Returns (seconds, bytes)."""
+    import numpy as np
+
+    import oracle
+    from block_quantized_wire_gb300.inputs import bf16_bits
+    xs, slices = pipe_inputs
+    xb = [bf16_bits(x[:rows]).reshape(-1) for x in xs]
+    sb = [bf16_bits(s[:slice_rows]) for s in slices]
+    n = xb[0].size
+    ns = sb[0].size
+    t0 = time.perf_counter()
+    qs = [oracle.quant_i8(b) for b in xb]
+    qa, sa, _ = oracle.dequant_accum_i8([q for q, _ in qs], [s for _, s in qs], materialize=False)
+    oracle.dequant_i8(qa, sa)
+    oracle.ring_hop_i8(qs[0][0], qs[0][1], xb[1])
+    C = HIDDEN * N_SLICES
+    qb = np.empty((slice_rows, C), np.uint8)
+    sbuf = np.empty((slice_rows, C // 32), np.uint8)
+    for i, s in enumerate(sb):
+        oracle.quant_mx_into(s, qb, sbuf, i * HIDDEN)
+    oracle.dequant_mx(qb, sbuf)
+    dt = time.perf_counter() - t0
+    nbytes = (W_SRC * kernel_bytes("quant_i8", n) + kernel_bytes("dequant_accum_i8", n) +
+              kernel_bytes("dequant_i8", n) + kernel_bytes("ring_hop_i8", n) +
+              N_SLICES * kernel_bytes("quant_mx", ns) + kernel_bytes("dequant_mx", ns * N_SLICES))
+    return dt, nbytes
+
+
+def cpu_inputs(rows: int, slice_rows: int):
+    """Workload inputs for the CPU oracle leg: the first rows of the GPU-drawn buffers
+    when a GPU exists (the very bits the GPU path consumes), else CPU draws."""
+    from block_quantized_wire_gb300 import inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    xs = [inputs.prefill_buffer(w, device=dev, rows=rows) for w in range(W_SRC)]
+    sl = inputs.mx_slices_4096(device=dev, rows=slice_rows)
+    return [x.cpu() for x in xs], [s.cpu() for s in sl]
+
+
+# ---------------------------------------------------------------- arms
+def run_bq(args, rank, world, local):
+    from block_quantized_wire_gb300 import build as bq_build
+    bq_build.build_library()
+    dev = torch.device("cuda", local)
+    pipe = Pipeline(args.rows, args.slice_rows, dev)
+    step_bytes = pipe.step_bytes()
+    nl = len(pipe.launches)
+    for _ in range(args.warmup):
+        pipe.run()
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        clk.mark_start()
+        start.record()
+        for k in range(args.steps):
+            pipe.run(events[k])
+        stop.record()
+        torch.cuda.synchronize()
+        clk.mark_stop()
+    barrier(world)
+    ms_local = start.elapsed_time(stop)
+    ms = max_over_ranks(ms_local, world)
+    ms_per_step = ms / args.steps
+
+    # per-kernel average launch duration (events on the launching stream)
+    per = {}
+    for k in range(args.steps):
+        prev = start if k == 0 else events[k - 1][nl - 1]
+        for i, (name, _, nbytes) in enumerate(pipe.launches):
+            t = prev.elapsed_time(events[k][i])
+            prev = events[k][i]
+            d = per.setdefault(name, {"ms": 0.0, "launches": 0, "bytes": nbytes})
+            d["ms"] += t
+            d["launches"] += 1
+    peak, peak_kind = load_peaks()
+    kernels = {}
+    for name, d in per.items():
+        avg_ms = d["ms"] / d["launches"]
+        gbs = d["bytes"] / (avg_ms * 1e-3) / 1e9
+        kernels[name] = {"launches_per_step": d["launches"] // args.steps, "avg_us": round(avg_ms * 1e3, 2),
+                         "bytes_per_launch": d["bytes"], "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "share": round(d["ms"] / (ms_local), 4)}
+    dominant = max(per, key=lambda k: per[k]["ms"])
+    dk = kernels[dominant]
+    traffic = None
+    tinfo = load_traffic().get(dominant)
+    scale = pipe.n / (65536 * HIDDEN) if dominant not in ("quant_mx", "dequant_mx") else 1.0
+    if tinfo and tinfo[0] == kernel_sources_sha() and args.rows == 65536:
+        traffic = int(tinfo[1] * scale)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GB/s"], "peak": peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": dk["frac"], "traffic": traffic,
+                "algorithmic_bytes": dk["bytes_per_launch"]}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pipe.host_buffers()
+        pipe.run_e2e()
+        torch.cuda.synchronize()
+        n_e2e = max(2, min(args.steps, args.e2e_steps))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n_e2e):
+            pipe.run_e2e()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
+        e2e = {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
+               "h2d_bytes_per_step": pipe.h2d, "d2h_bytes_per_step": pipe.d2h, "ms_per_step": round(e_ms, 3),
+               "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ci = (pipe.xs, pipe.slices)
+        r, sr = args.cpu_rows, args.cpu_slice_rows
+        dt, nb = oracle_sample(([x[:r].cpu() for x in ci[0]], [s[:sr].cpu() for s in ci[1]]), r, sr)
+        cpu = {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"one step of the same pipeline on the first {r} of {args.rows} rows of each INT8 buffer "
+                         f"and the first {sr} of {args.slice_rows} rows of each MX slice "
+                         f"({nb} algorithmic bytes, {dt:.2f} s, single thread)"}
+
+    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"prefill pipeline: 4 x BF16 {args.rows}x{HIDDEN} quant_i8 -> dequant_accum_i8 (W=4) "
+                               f"-> dequant_i8, ring_hop_i8; 6 x BF16 {args.slice_rows}x{HIDDEN} quant_mx staged into "
+                               f"{args.slice_rows}x{HIDDEN * N_SLICES}, dequant_mx",
+                   "step_bytes": step_bytes, "launches_per_step": nl,
+                   "l2": "no flush: step working set ~12.5 GB >> 129 MB L2",
+                   "parallelism": f"replicas x{world} (no collective)"},
+        "roofline": roofline, "kernels": kernels, "clocks": clocks,
+        "e2e": e2e, "gpu_launches": nl * args.steps, "cpu_baseline": cpu,
+        "device": torch.cuda.get_device_name(dev),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world, local):
+    if rank != 0:
+        return
+    cores = 1
+    # calibrate a sample so that warmup + steps finish in about args.ref_budget seconds
+    rows, srows = 16, 4
+    ci = cpu_inputs(max(rows, 256), max(srows, 64))
+    dt, nb = oracle_sample(ci, rows, srows)
+    per_step = max(0.05, min(3.0, args.ref_budget / max(1, args.steps + args.warmup)))
+    factor = max(1.0, per_step / max(dt, 1e-3))
+    rows = int(min(256, max(16, rows * factor)))
+    srows = int(min(64, max(4, srows * factor)))
+    for _ in range(args.warmup):
+        oracle_sample(ci, rows, srows)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample(ci, rows, srows)
+        tot_t += dt
+        tot_b += nb
+    value = tot_b / tot_t / 1e9
+    sample = (f"each step: the full step's operations on the first {rows} of 65536 rows of each INT8 buffer and the "
+              f"first {srows} of 4096 rows of each MX slice ({nb} algorithmic bytes), single thread")
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "prefill pipeline (sampled rows), same operations as the bq arm"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": cores, "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["bq", "reference"], default="bq")
+    ap.add_argument("--rows", type=int, default=65536, help="rows of each INT8 buffer (65536 = the benchmark)")
+    ap.add_argument("--slice-rows", type=int, default=4096, help="rows of each MX slice (4096 = the benchmark)")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-slice-rows", type=int, default=256)
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of CPU work for --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if world > 1 and world != args.gpus:
+        print(f"bench: WORLD_SIZE={world} differs from --gpus {args.gpus}; using {world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world, local)
+        else:
+            run_bq(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,73 @@
+"""ctypes loader for libbq.so (the C ABI declared in include/bq.h).
+
+There is no fallback: if the library is missing or does not load, every codec call
+raises. Build it with ``block_quantized_wire_gb300.build.build_library()`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+BQ_OK = 0
+STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_ALIAS",
+                5: "BQ_ERR_CUDA"}
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_PROTOS = {
+    "bq_abi_version": ([], ctypes.c_int),
+    "bq_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "bq_wire_bytes": ([_I64], _I64),
+    "bq_quant_i8": ([_P, _I64, _P, _P, _P], ctypes.c_int),
+    "bq_dequant_i8": ([_P, _P, _I64, _P, _P], ctypes.c_int),
+    "bq_dequant_accum_i8": ([_P, _P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
+    "bq_ring_hop_i8": ([_P, _P, _P, _I64, _P, _P, _P, _P], ctypes.c_int),
+    "bq_quant_mx": ([_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
+    "bq_dequant_mx": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+}
+
+
+class BQError(RuntimeError):
+    """A bq_* call returned a non-OK status."""
+
+    def __init__(self, func: str, status: int, message: str):
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)} ({message})")
+        self.func = func
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libbq.so once; raise if it is not built or does not load."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(
+                    f"libbq.so is not built ({path}); run block_quantized_wire_gb300.build.build_library()")
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in _PROTOS.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            if lib.bq_abi_version() != 1:
+                raise ImportError(f"libbq.so ABI version {lib.bq_abi_version()} != 1")
+            _lib = lib
+    return _lib
+
+
+def check(func: str, status: int) -> None:
+    if status != BQ_OK:
+        msg = load().bq_status_string(status).decode()
+        raise BQError(func, status, msg)

@@ -1,0 +1,157 @@
+"""Python binding of the codec calls: torch tensors in, C ABI call out.
+
+Every function only checks dtypes/devices/strides, reads pointers and the current
+CUDA stream, and calls the same-named ``bq_*`` entry point of libbq.so; all
+arithmetic runs in the library's kernels. Outputs are caller-owned tensors written in
+place; nothing is allocated here except by the explicit ``empty_*`` helpers.
+
+Wire layout (include/bq.h): an n-value INT8 wire is ``q`` (int8 [n]) followed by
+``scales`` (float32 [n/128]); an MXFP8 tensor [rows, cols] is ``q`` (uint8 E4M3
+[rows, cols]) and ``s`` (uint8 E8M0 [rows, cols/32]).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from ._lib import check, load
+
+BLOCK_I8 = 128
+GROUP_MX = 32
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _flat(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _rows(t: torch.Tensor, dtype: torch.dtype, name: str):
+    """(pointer, rows, cols, leading dimension in elements) of a row-major 2-D view."""
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name}: expected a 2-D row-major view with unit column stride")
+    ld = t.stride(0) if t.shape[0] > 1 else t.shape[1]
+    return t.data_ptr(), t.shape[0], t.shape[1], ld
+
+
+# ---------------------------------------------------------------- allocation helpers
+def wire_bytes(n: int) -> int:
+    """132 bytes per 128 values (bq_wire_bytes)."""
+    r = load().bq_wire_bytes(n)
+    if r < 0:
+        raise ValueError(f"wire_bytes: n={n} is not a non-negative multiple of 128")
+    return r
+
+
+def empty_wire_i8(n: int, device="cuda"):
+    """One contiguous n-value INT8 wire buffer, returned as (buffer, q view, scales view)."""
+    nbytes = wire_bytes(n)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    q = buf[:n].view(torch.int8)
+    s = buf[n:].view(torch.float32)
+    return buf, q, s
+
+
+def empty_mx(rows: int, cols: int, device="cuda"):
+    """(E4M3 values [rows, cols], E8M0 scales [rows, cols/32]) for an MXFP8 tensor."""
+    return (torch.empty((rows, cols), dtype=torch.uint8, device=device),
+            torch.empty((rows, cols // GROUP_MX), dtype=torch.uint8, device=device))
+
+
+# ---------------------------------------------------------------- block INT8
+def quant_i8(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """BF16 x [n] -> payload q [n] (int8) + scales [n/128] (float32)."""
+    n = x.numel()
+    if q.numel() != n or scales.numel() * BLOCK_I8 != n:
+        raise ValueError("quant_i8: output sizes do not match x")
+    check("bq_quant_i8", load().bq_quant_i8(
+        _flat(x, torch.bfloat16, "x"), n, _flat(q, torch.int8, "q"), _flat(scales, torch.float32, "scales"),
+        _stream(stream)))
+
+
+def dequant_i8(q: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """payload q [n] + scales [n/128] -> BF16 out [n]."""
+    n = q.numel()
+    if out.numel() != n or scales.numel() * BLOCK_I8 != n:
+        raise ValueError("dequant_i8: sizes do not match")
+    check("bq_dequant_i8", load().bq_dequant_i8(
+        _flat(q, torch.int8, "q"), _flat(scales, torch.float32, "scales"), n, _flat(out, torch.bfloat16, "out"),
+        _stream(stream)))
+
+
+def dequant_accum_i8(q_srcs: Sequence[torch.Tensor], scale_srcs: Sequence[torch.Tensor], q_out: torch.Tensor,
+                     scales_out: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Sum W dequantized sources in FP32 in list order, requantize into q_out/scales_out;
+    optionally materialize the new payload into out (BF16)."""
+    W = len(q_srcs)
+    if W != len(scale_srcs):
+        raise ValueError("dequant_accum_i8: q_srcs and scale_srcs differ in length")
+    n = q_out.numel()
+    for q, s in zip(q_srcs, scale_srcs):
+        if q.numel() != n or s.numel() * BLOCK_I8 != n:
+            raise ValueError("dequant_accum_i8: a source's size differs from the output's")
+    if scales_out.numel() * BLOCK_I8 != n or (out is not None and out.numel() != n):
+        raise ValueError("dequant_accum_i8: output sizes do not match")
+    qp = (ctypes.c_void_p * max(W, 1))(*[_flat(q, torch.int8, "q_srcs[]") for q in q_srcs])
+    sp = (ctypes.c_void_p * max(W, 1))(*[_flat(s, torch.float32, "scale_srcs[]") for s in scale_srcs])
+    check("bq_dequant_accum_i8", load().bq_dequant_accum_i8(
+        ctypes.cast(qp, ctypes.c_void_p), ctypes.cast(sp, ctypes.c_void_p), W, n,
+        _flat(q_out, torch.int8, "q_out"), _flat(scales_out, torch.float32, "scales_out"),
+        _flat(out, torch.bfloat16, "out") if out is not None else None, _stream(stream)))
+
+
+def ring_hop_i8(q_in: torch.Tensor, s_in: torch.Tensor, x_local: torch.Tensor, q_out: torch.Tensor,
+                s_out: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Fused hop: requant(dequant(q_in, s_in) + x_local) -> q_out/s_out; optional BF16 out."""
+    n = q_in.numel()
+    if x_local.numel() != n or q_out.numel() != n or s_in.numel() * BLOCK_I8 != n or \
+            s_out.numel() * BLOCK_I8 != n or (out is not None and out.numel() != n):
+        raise ValueError("ring_hop_i8: sizes do not match")
+    check("bq_ring_hop_i8", load().bq_ring_hop_i8(
+        _flat(q_in, torch.int8, "q_in"), _flat(s_in, torch.float32, "s_in"),
+        _flat(x_local, torch.bfloat16, "x_local"), n, _flat(q_out, torch.int8, "q_out"),
+        _flat(s_out, torch.float32, "s_out"), _flat(out, torch.bfloat16, "out") if out is not None else None,
+        _stream(stream)))
+
+
+# ---------------------------------------------------------------- MXFP8
+def quant_mx(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
+    """BF16 x [rows, cols] -> E4M3 q [rows, cols] + E8M0 s [rows, cols/32].
+
+    Any of the three may be a column slice of a wider row-major buffer, e.g.
+    ``q_buf[:, c0:c0+cols]`` and ``s_buf[:, c0//32:(c0+cols)//32]`` with c0 % 128 == 0.
+    """
+    xp, rows, cols, ld_x = _rows(x, torch.bfloat16, "x")
+    qp, qr, qc, ld_q = _rows(q, torch.uint8, "q")
+    sp, sr, sc, ld_s = _rows(s, torch.uint8, "s")
+    if (qr, qc) != (rows, cols) or (sr, sc) != (rows, cols // GROUP_MX):
+        raise ValueError("quant_mx: output shapes do not match x")
+    check("bq_quant_mx", load().bq_quant_mx(xp, rows, cols, ld_x, qp, ld_q, sp, ld_s, _stream(stream)))
+
+
+def dequant_mx(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """E4M3 q [rows, cols] + E8M0 s [rows, cols/32] -> BF16 out [rows, cols]."""
+    qp, rows, cols, ld_q = _rows(q, torch.uint8, "q")
+    sp, sr, sc, ld_s = _rows(s, torch.uint8, "s")
+    op, orr, oc, ld_o = _rows(out, torch.bfloat16, "out")
+    if (sr, sc) != (rows, cols // GROUP_MX) or (orr, oc) != (rows, cols):
+        raise ValueError("dequant_mx: shapes do not match")
+    check("bq_dequant_mx", load().bq_dequant_mx(qp, ld_q, sp, ld_s, rows, cols, op, ld_o, _stream(stream)))

@@ -1,0 +1,222 @@
+// C ABI of libbq.so: argument checks (all before any CUDA call) and kernel dispatch.
+// The operations and conventions are specified in include/bq.h.
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "bq.h"
+#include "bq_launch.h"
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range span(const void *p, int64_t bytes)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+// Bounding interval of a row-major strided region: rows of `row_bytes`, `ld_bytes` apart.
+Range span2d(const void *p, int64_t rows, int64_t row_bytes, int64_t ld_bytes)
+{
+    return span(p, (rows - 1) * ld_bytes + row_bytes);
+}
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Outputs must be disjoint from each other and from every input.
+bool any_alias(const Range *outs, int n_out, const Range *ins, int n_in)
+{
+    for (int i = 0; i < n_out; i++) {
+        for (int j = i + 1; j < n_out; j++)
+            if (overlap(outs[i], outs[j])) return true;
+        for (int j = 0; j < n_in; j++)
+            if (overlap(outs[i], ins[j])) return true;
+    }
+    return false;
+}
+
+bq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BQ_OK : BQ_ERR_CUDA; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ launch sizing
+namespace bqk {
+
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int kMaxKernels = 32;
+std::atomic<int> g_sms[kMaxDevices];
+struct OccEntry {
+    const void *kernel;
+    int ctas_per_sm;
+};
+OccEntry g_occ[kMaxKernels];
+int g_occ_n = 0;
+std::mutex g_occ_mu;
+}  // namespace
+
+cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid)
+{
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev)) return e;
+    int sms = (dev >= 0 && dev < kMaxDevices) ? g_sms[dev].load(std::memory_order_relaxed) : 0;
+    if (sms == 0) {
+        if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) return e;
+        if (dev >= 0 && dev < kMaxDevices) g_sms[dev].store(sms, std::memory_order_relaxed);
+    }
+    int occ = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_occ_mu);
+        for (int i = 0; i < g_occ_n; i++)
+            if (g_occ[i].kernel == kernel) occ = g_occ[i].ctas_per_sm;
+    }
+    if (occ == 0) {
+        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0)) return e;
+        if (occ < 1) occ = 1;
+        std::lock_guard<std::mutex> lock(g_occ_mu);
+        if (g_occ_n < kMaxKernels) g_occ[g_occ_n++] = OccEntry{kernel, occ};
+    }
+    const int64_t warps_per_cta = kThreads / 32;
+    const int64_t need = (nchunk + warps_per_cta - 1) / warps_per_cta;
+    const int64_t full = static_cast<int64_t>(sms) * occ;
+    *grid = static_cast<int>(need < full ? (need > 0 ? need : 1) : full);
+    return cudaSuccess;
+}
+
+}  // namespace bqk
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+int bq_abi_version(void) { return BQ_ABI_VERSION; }
+
+const char *bq_status_string(int status)
+{
+    switch (status) {
+    case BQ_OK: return "ok";
+    case BQ_ERR_NULL: return "a required pointer is NULL";
+    case BQ_ERR_SHAPE: return "size not a multiple of 128, negative, W out of range, or leading dimension too small";
+    case BQ_ERR_ALIGN: return "pointer or leading dimension breaks the alignment rules";
+    case BQ_ERR_ALIAS: return "an output overlaps an input or another output";
+    case BQ_ERR_CUDA: return "the CUDA runtime reported an error for the launch";
+    default: return "unknown status";
+    }
+}
+
+int64_t bq_wire_bytes(int64_t n)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return -1;
+    return n + 4 * (n / BQ_BLOCK_I8);
+}
+
+bq_status bq_quant_i8(const void *x_bf16, int64_t n, int8_t *q, float *scales, cudaStream_t stream)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!x_bf16 || !q || !scales) return BQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(scales, 4)) return BQ_ERR_ALIGN;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    const Range ins[] = {span(x_bf16, 2 * n)};
+    const Range outs[] = {span(q, n), span(scales, 4 * nblk)};
+    if (any_alias(outs, 2, ins, 1)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_quant_i8(static_cast<const uint16_t *>(x_bf16), nblk, q, scales, stream));
+}
+
+bq_status bq_dequant_i8(const int8_t *q, const float *scales, int64_t n, void *out_bf16, cudaStream_t stream)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!q || !scales || !out_bf16) return BQ_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(scales, 4) || !aligned(out_bf16, 16)) return BQ_ERR_ALIGN;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    const Range ins[] = {span(q, n), span(scales, 4 * nblk)};
+    const Range outs[] = {span(out_bf16, 2 * n)};
+    if (any_alias(outs, 1, ins, 2)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_dequant_i8(q, scales, nblk, static_cast<uint16_t *>(out_bf16), stream));
+}
+
+bq_status bq_dequant_accum_i8(const int8_t *const *q_srcs, const float *const *scale_srcs, int W, int64_t n,
+                              int8_t *q_out, float *scales_out, void *out_bf16, cudaStream_t stream)
+{
+    if (W < 1 || W > BQ_MAX_W) return BQ_ERR_SHAPE;
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!q_srcs || !scale_srcs || !q_out || !scales_out) return BQ_ERR_NULL;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    bqk::SourceList src = {};
+    Range ins[2 * BQ_MAX_W];
+    for (int w = 0; w < W; w++) {
+        if (!q_srcs[w] || !scale_srcs[w]) return BQ_ERR_NULL;
+        if (!aligned(q_srcs[w], 16) || !aligned(scale_srcs[w], 4)) return BQ_ERR_ALIGN;
+        src.q[w] = q_srcs[w];
+        src.s[w] = scale_srcs[w];
+        ins[2 * w] = span(q_srcs[w], n);
+        ins[2 * w + 1] = span(scale_srcs[w], 4 * nblk);
+    }
+    if (!aligned(q_out, 16) || !aligned(scales_out, 4) || (out_bf16 && !aligned(out_bf16, 16))) return BQ_ERR_ALIGN;
+    Range outs[3] = {span(q_out, n), span(scales_out, 4 * nblk), {}};
+    int n_out = 2;
+    if (out_bf16) outs[n_out++] = span(out_bf16, 2 * n);
+    if (any_alias(outs, n_out, ins, 2 * W)) return BQ_ERR_ALIAS;
+    return from_cuda(
+        bqk::launch_accum_i8(src, W, nblk, q_out, scales_out, static_cast<uint16_t *>(out_bf16), stream));
+}
+
+bq_status bq_ring_hop_i8(const int8_t *q_in, const float *s_in, const void *x_local_bf16, int64_t n, int8_t *q_out,
+                         float *s_out, void *out_bf16, cudaStream_t stream)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!q_in || !s_in || !x_local_bf16 || !q_out || !s_out) return BQ_ERR_NULL;
+    if (!aligned(q_in, 16) || !aligned(s_in, 4) || !aligned(x_local_bf16, 16) || !aligned(q_out, 16) ||
+        !aligned(s_out, 4) || (out_bf16 && !aligned(out_bf16, 16)))
+        return BQ_ERR_ALIGN;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    const Range ins[] = {span(q_in, n), span(s_in, 4 * nblk), span(x_local_bf16, 2 * n)};
+    Range outs[3] = {span(q_out, n), span(s_out, 4 * nblk), {}};
+    int n_out = 2;
+    if (out_bf16) outs[n_out++] = span(out_bf16, 2 * n);
+    if (any_alias(outs, n_out, ins, 3)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_ring_hop_i8(q_in, s_in, static_cast<const uint16_t *>(x_local_bf16), nblk, q_out,
+                                             s_out, static_cast<uint16_t *>(out_bf16), stream));
+}
+
+bq_status bq_quant_mx(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q_e4m3, int64_t ld_q,
+                      uint8_t *s_e8m0, int64_t ld_s, cudaStream_t stream)
+{
+    if (rows < 0 || cols < 0 || cols % 128) return BQ_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return BQ_OK;
+    if (ld_x < cols || ld_q < cols || ld_s < cols / BQ_GROUP_MX) return BQ_ERR_SHAPE;
+    if (!x_bf16 || !q_e4m3 || !s_e8m0) return BQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || ld_x % 8 || !aligned(q_e4m3, 16) || ld_q % 16 || !aligned(s_e8m0, 4) || ld_s % 4)
+        return BQ_ERR_ALIGN;
+    const Range ins[] = {span2d(x_bf16, rows, 2 * cols, 2 * ld_x)};
+    const Range outs[] = {span2d(q_e4m3, rows, cols, ld_q), span2d(s_e8m0, rows, cols / BQ_GROUP_MX, ld_s)};
+    if (any_alias(outs, 2, ins, 1)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_quant_mx(static_cast<const uint16_t *>(x_bf16), ld_x, rows, cols, q_e4m3, ld_q,
+                                          s_e8m0, ld_s, stream));
+}
+
+bq_status bq_dequant_mx(const uint8_t *q_e4m3, int64_t ld_q, const uint8_t *s_e8m0, int64_t ld_s, int64_t rows,
+                        int64_t cols, void *out_bf16, int64_t ld_out, cudaStream_t stream)
+{
+    if (rows < 0 || cols < 0 || cols % 128) return BQ_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return BQ_OK;
+    if (ld_q < cols || ld_s < cols / BQ_GROUP_MX || ld_out < cols) return BQ_ERR_SHAPE;
+    if (!q_e4m3 || !s_e8m0 || !out_bf16) return BQ_ERR_NULL;
+    if (!aligned(q_e4m3, 16) || ld_q % 16 || !aligned(s_e8m0, 4) || ld_s % 4 || !aligned(out_bf16, 16) || ld_out % 8)
+        return BQ_ERR_ALIGN;
+    const Range ins[] = {span2d(q_e4m3, rows, cols, ld_q), span2d(s_e8m0, rows, cols / BQ_GROUP_MX, ld_s)};
+    const Range outs[] = {span2d(out_bf16, rows, 2 * cols, 2 * ld_out)};
+    if (any_alias(outs, 1, ins, 2)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_dequant_mx(q_e4m3, ld_q, s_e8m0, ld_s, rows, cols, static_cast<uint16_t *>(out_bf16),
+                                            ld_out, stream));
+}
+
+}  // extern "C"

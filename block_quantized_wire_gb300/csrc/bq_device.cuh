@@ -1,0 +1,258 @@
+// Device-side building blocks shared by the codec kernels (sm_103a).
+//
+// Work decomposition used by every kernel: a warp owns a "chunk" of kChunkBlocks
+// 128-value blocks per loop iteration. The chunk is read as kSegs warp-wide
+// "segments" of 256 values: in segment j, half-warp h (lanes 16h..16h+15) holds
+// block 2j+h of the chunk, each lane 8 consecutive values. So every warp-wide access
+// is one contiguous run (512 B of BF16, 256 B of INT8/E4M3), block amax is a
+// 16-lane shuffle reduction (4 lanes for a 32-value MX group), and the chunk's
+// kChunkBlocks scales are written by lanes 0..kChunkBlocks-1 in one coalesced store.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "bq_launch.h"
+
+namespace bqk {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kSegs = 4;                      // segments per warp iteration
+constexpr int kChunkBlocks = 2 * kSegs;       // 128-value blocks per warp iteration
+constexpr float kFltMin = 1.17549435e-38f;    // smallest normal binary32
+
+// ---------------------------------------------------------------- global memory
+// Inputs are read once: non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
+{
+    uint32_t r;
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void *p, uint2 v)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_u32(void *p, uint32_t v)
+{
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- number formats
+// Eight BF16 values (one 16-byte word) widened exactly to binary32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float (&v)[8])
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        v[2 * i] = __uint_as_float(u[i] << 16);
+        v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+
+// Two binary32 values rounded to nearest-even BF16, packed (lo in bits 0..15).
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16x8(const float (&v)[8])
+{
+    return make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]),
+                      f32x2_to_bf16x2(v[4], v[5]), f32x2_to_bf16x2(v[6], v[7]));
+}
+
+// Low bytes of four 32-bit words, packed little-endian into one word.
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// Four signed payload bytes (one word) -> their exact binary32 values. Each byte,
+// offset by 128, is placed in the low mantissa bits of 2^23 and the offset removed:
+// (2^23 + q + 128) - (2^23 + 128) = q exactly; q = 0 gives +0.
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *v)
+{
+    constexpr float kBias = 8388736.0f;  // 2^23 + 128
+    const uint32_t u = w ^ 0x80808080u;
+    v[0] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7540)), kBias);
+    v[1] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7541)), kBias);
+    v[2] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7542)), kBias);
+    v[3] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7543)), kBias);
+}
+
+__device__ __forceinline__ void i8x8_to_f32(uint2 w, float (&v)[8])
+{
+    i8x4_to_f32(w.x, v);
+    i8x4_to_f32(w.y, v + 4);
+}
+
+// ---------------------------------------------------------------- block INT8 scale
+// s = fl(amax / 127). For a normal s the quotients x/s are formed as x * fl(1/s) and
+// checked (see i8_quant8); a subnormal s (tiny FP32 sums only) takes the exact path
+// for the whole block; s == 0 gives payload 0 (r = 0 makes every t zero).
+struct I8Scale {
+    float s;
+    float r;
+    bool exact_only;
+};
+
+__device__ __forceinline__ I8Scale i8_scale(float amax)
+{
+    I8Scale b;
+    b.s = __fdiv_rn(amax, 127.0f);
+    const bool normal = b.s >= kFltMin;
+    b.r = normal ? __frcp_rn(b.s) : 0.0f;
+    b.exact_only = (b.s > 0.0f) && !normal;
+    return b;
+}
+
+// Quantize eight values of one block. Returns the payload bytes (value i in byte i)
+// and leaves the integers, as binary32 (+0 for zero), in qf for a fused
+// materialization.
+//
+// Fast path (s normal): t = fl(x * fl(1/s)) differs from x/s by less than 2^-15 (|x/s|
+// <= 127.00002, two roundings of relative 2^-24 each), and fl(x/s) differs from x/s
+// by at most 2^-18, so |t - fl(x/s)| < 2^-14. When t is farther than 2^-14 from every
+// half-integer, t and fl(x/s) round to the same integer; adding 1.5 * 2^23 performs
+// that rounding (ties to even) and leaves the integer in the low mantissa bits, whose
+// low byte is the two's-complement payload byte. Otherwise (about 1 value in 8000)
+// the lane recomputes its eight values with the IEEE division x / s.
+__device__ __forceinline__ uint2 i8_quant8(const float (&v)[8], const I8Scale &b, float (&qf)[8])
+{
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr float kNearHalf = 0.49993896484375f;  // 1/2 - 2^-14
+    uint32_t w[8];
+    float dmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const float t = __fmul_rn(v[i], b.r);
+        const float y = __fadd_rn(t, kMagic);
+        const float k = __fsub_rn(y, kMagic);
+        dmax = fmaxf(dmax, fabsf(__fsub_rn(t, k)));
+        w[i] = __float_as_uint(y);
+        qf[i] = k;
+    }
+    if (dmax > kNearHalf || b.exact_only) {
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            float k = 0.0f;
+            if (b.s != 0.0f) {
+                k = rintf(__fdiv_rn(v[i], b.s));
+                k = fminf(fmaxf(k, -127.0f), 127.0f);
+            }
+            const float y = __fadd_rn(k, kMagic);
+            w[i] = __float_as_uint(y);
+            qf[i] = __fsub_rn(y, kMagic);  // canonical: -0 becomes +0
+        }
+    }
+    return make_uint2(pack_low_bytes(w[0], w[1], w[2], w[3]), pack_low_bytes(w[4], w[5], w[6], w[7]));
+}
+
+__device__ __forceinline__ float amax8(const float (&v)[8])
+{
+    float m = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < 8; i++) m = fmaxf(m, fabsf(v[i]));
+    return m;
+}
+
+// max over the 16 lanes of a half-warp (xor partners stay inside the half)
+__device__ __forceinline__ float halfwarp_max(float m)
+{
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+    return m;
+}
+
+// BF16 of fl(q * s) for eight integers held as binary32.
+__device__ __forceinline__ uint4 i8_materialize8(const float (&qf)[8], float s)
+{
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) d[i] = __fmul_rn(qf[i], s);
+    return f32x8_to_bf16x8(d);
+}
+
+// ---------------------------------------------------------------- MXFP8
+// E8M0 byte for a group: 127 for amax == 0, else the smallest e in [0, 254] with
+// 2^(e-127) >= v = fl(amax / 448). From v's binary32 fields: a normal v with exponent
+// field E is 2^(E-127) when its fraction is zero (e = E) and lies strictly between
+// 2^(E-127) and 2^(E-126) otherwise (e = E + 1); a subnormal v is at most 2^-127
+// (e = 0) when its fraction field is <= 2^22, else in (2^-127, 2^-126) (e = 1).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax)
+{
+    if (amax == 0.0f) return 127u;
+    const uint32_t u = __float_as_uint(__fdiv_rn(amax, 448.0f));
+    const uint32_t ex = u >> 23;
+    const uint32_t fr = u & 0x7fffffu;
+    uint32_t e = (ex == 0u) ? (fr > 0x400000u ? 1u : 0u) : ex + (fr != 0u ? 1u : 0u);
+    return e > 254u ? 254u : e;
+}
+
+// 2^k as binary32 for k in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float exp2i(int k)
+{
+    return k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Eight binary32 values -> eight E4M3 codes (nearest even, saturating), value i in
+// byte i.
+__device__ __forceinline__ uint2 f32x8_to_e4m3x8(const float (&y)[8])
+{
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        h[i] = __nv_cvt_float2_to_fp8x2(make_float2(y[2 * i], y[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+// Eight E4M3 codes -> their exact binary32 values, each times 2^k (exact).
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float p, float (&v)[8])
+{
+    const uint32_t u[2] = {w.x, w.y};
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const __nv_fp8x2_storage_t c = static_cast<__nv_fp8x2_storage_t>((u[j] >> (16 * i)) & 0xffffu);
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+            const __half2 hh = *reinterpret_cast<const __half2 *>(&hr);
+            const float2 f = __half22float2(hh);
+            v[4 * j + 2 * i] = __fmul_rn(f.x, p);
+            v[4 * j + 2 * i + 1] = __fmul_rn(f.y, p);
+        }
+    }
+}
+
+}  // namespace bqk

@@ -1,0 +1,37 @@
+// Internal launcher interface between the C ABI (bq_api.cu) and the kernels.
+// Arguments are already validated; every launcher only enqueues work on `stream`
+// and returns the launch's cudaError_t.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace bqk {
+
+constexpr int kThreads = 256;  // threads per CTA (8 warps) for every codec kernel
+constexpr int kMaxSources = 16;
+
+struct SourceList {
+    const int8_t *q[kMaxSources];
+    const float *s[kMaxSources];
+};
+
+cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st);
+cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out,
+                              cudaStream_t st);
+cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *q, float *s,
+                            uint16_t *out, cudaStream_t st);
+cudaError_t launch_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint16_t *x, int64_t nblk,
+                               int8_t *q, float *s, uint16_t *out, cudaStream_t st);
+cudaError_t launch_quant_mx(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,
+                            int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t st);
+cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_s,
+                              int64_t rows, int64_t cols, uint16_t *out, int64_t ld_out,
+                              cudaStream_t st);
+
+// Grid size for a grid-stride kernel over `nchunk` warp chunks: enough CTAs to fill
+// every SM of the current device at the kernel's occupancy, and no more CTAs than
+// there are chunks. Returns the error of the device queries, if any.
+cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid);
+
+}  // namespace bqk

@@ -1,0 +1,92 @@
+"""The pages' three INT8 wire topologies, simulated on one GPU.
+
+W "ranks" are W buffers resident in one GPU's memory; moving a payload from one rank
+to another is handing over the same device tensor, so there is no transport and no
+collective. Each topology is a host loop over the codec calls of ``codec``; it adds no
+kernels of its own.
+
+From "feat(pcie_dma): add block-INT8 wire modes for AG, ring, and A2A", Summary:
+``i8`` (BF16 reduce-scatter, INT8 all-gather: here the quantize -> materialize round
+trip of one shard), ``i8_ring`` (INT8 reduce-scatter ring: the fused hop at every
+step, then an INT8 all-gather), ``i8_a2a`` (each rank quantizes once, the shard owner
+accumulates all sources in FP32 and requantizes, then an INT8 broadcast); in every
+topology the owner materializes from the same final payload it forwards.
+"""
+from __future__ import annotations
+
+from typing import List, Sequence
+
+import torch
+
+from . import codec
+
+
+def i8_roundtrip(x: torch.Tensor, stream=None):
+    """Quantize one BF16 tensor and materialize it: (payload, scales, BF16)."""
+    n = x.numel()
+    _, q, s = codec.empty_wire_i8(n, x.device)
+    out = torch.empty_like(x)
+    codec.quant_i8(x, q, s, stream)
+    codec.dequant_i8(q, s, out, stream)
+    return q, s, out
+
+
+def i8_a2a(xs: Sequence[torch.Tensor], stream=None):
+    """Quantize-once all-to-all for one owner: every source is quantized, the owner sums
+    the W payloads in source order and requantizes (the broadcast payload), and
+    materializes it. Returns (payload, scales, owner BF16, per-source payloads)."""
+    n = xs[0].numel()
+    srcs = []
+    for x in xs:
+        _, q, s = codec.empty_wire_i8(n, x.device)
+        codec.quant_i8(x, q, s, stream)
+        srcs.append((q, s))
+    _, q_out, s_out = codec.empty_wire_i8(n, xs[0].device)
+    owner = torch.empty_like(xs[0])
+    codec.dequant_accum_i8([q for q, _ in srcs], [s for _, s in srcs], q_out, s_out, owner, stream)
+    return q_out, s_out, owner, srcs
+
+
+def ring_order(shard: int, W: int) -> List[int]:
+    """Ranks visited by shard `shard`'s reduce-scatter chain: it starts at the rank after
+    the owner, which quantizes its own copy, and every later rank adds its copy with a
+    fused hop; the last hop runs on the owner (rank `shard`)."""
+    return [(shard + 1 + k) % W for k in range(W)]
+
+
+def i8_ring(xs: Sequence[torch.Tensor], stream=None):
+    """INT8 reduce-scatter ring + INT8 all-gather over W rank buffers.
+
+    Every buffer [rows, cols] is split into W contiguous row shards. For shard c the
+    chain of ring_order(c, W) runs one quantize and W-1 fused hops, the last (at the
+    owner c) also materializing the owner's BF16. Then every rank materializes all W
+    final payloads into its own full-size output (the all-gather).
+    Returns (per-rank BF16 outputs, final payloads [(q, s)] per shard, owner BF16 per shard).
+    """
+    W = len(xs)
+    rows = xs[0].shape[0]
+    if rows % W:
+        raise ValueError("i8_ring: rows must divide evenly into W shards")
+    shard_rows = rows // W
+    shards = [[x[c * shard_rows:(c + 1) * shard_rows] for c in range(W)] for x in xs]
+    n = shards[0][0].numel()
+    finals, owners = [], []
+    for c in range(W):
+        chain = ring_order(c, W)
+        _, q, s = codec.empty_wire_i8(n, xs[0].device)
+        codec.quant_i8(shards[chain[0]][c], q, s, stream)
+        owner = torch.empty_like(shards[0][c])
+        for step, rank in enumerate(chain[1:], start=1):
+            _, q2, s2 = codec.empty_wire_i8(n, xs[0].device)
+            last = step == W - 1
+            codec.ring_hop_i8(q, s, shards[rank][c], q2, s2, owner if last else None, stream)
+            q, s = q2, s2
+        finals.append((q, s))
+        owners.append(owner)
+    outs = []
+    for _rank in range(W):
+        out = torch.empty_like(xs[0])
+        for c in range(W):
+            codec.dequant_i8(finals[c][0], finals[c][1], out[c * shard_rows:(c + 1) * shard_rows], stream)
+        outs.append(out)
+    return outs, finals, owners

@@ -1,0 +1,170 @@
+/*
+ * bq.h — C ABI of libbq.so, the block-quantized wire codec for GB300 (sm_103a).
+ *
+ * The codec compresses BF16 all-reduce payloads into two wire formats, each 132
+ * bytes per 128 values:
+ *
+ *   block INT8   128 signed payload bytes + one FP32 scale = amax/127 per block of
+ *                128 consecutive values ("feat(pcie_dma): add block-INT8 wire modes
+ *                for AG, ring, and A2A", Summary);
+ *   MXFP8        E4M3 values + one E8M0 scale byte per 32 consecutive values of a
+ *                row ("feat(pcie_dma): add INT8 and MXFP8 wire modes", Summary).
+ *
+ * Wire layout of an n-value tensor (n % 128 == 0). The pages fix the size of a block
+ * (132 bytes) but not how payload and scales interleave; this library keeps them in
+ * two regions so that both can be moved with 16-byte vector accesses:
+ *   INT8   payload  int8_t  q[n]          value i in block i/128
+ *          scales   float   s[n/128]      little-endian IEEE binary32
+ *   MXFP8  values   uint8_t q[rows][ld_q] E4M3 codes (OCP: bias 7, max 448)
+ *          scales   uint8_t s[rows][ld_s] E8M0 byte e stands for 2^(e-127);
+ *                                         s[r][g] covers columns [32g, 32g+32)
+ * A caller that wants one contiguous wire buffer places the scale region directly
+ * after the payload region (byte offset n, which keeps 16-byte alignment).
+ *
+ * Arithmetic (bit-exact; no fused multiply-add anywhere):
+ *   quantize   amax = max |x| over the block; s = fl(amax / 127) (IEEE binary32
+ *              division, round to nearest even); q = nearest integer to fl(x / s),
+ *              ties to even, clamped to [-127, 127]; a block with s == 0 (all-zero
+ *              block) has q == 0.
+ *   materialize  out = BF16_rne(fl((float)q * s)) — a binary32 product, then BF16.
+ *   accumulate   d_w = fl(q_w * s_w); acc = (((d_0 + d_1) + d_2) + ...) in binary32
+ *              in source order; acc is requantized as above.
+ *   ring hop   v = fl(fl(q_in * s_in) + x_local), requantized as above.
+ *   MX scale   all-zero group -> 127; else the smallest e in [0, 254] with
+ *              2^(e-127) >= fl(amax / 448) ("feat(pcie_dma): add INT8 and MXFP8 wire
+ *              modes", review comment on mxfp8_scale_byte: round toward +inf,
+ *              saturating).
+ *   MX values  code = E4M3_rne_satfinite(x * 2^(127-e)); the sign of zero is kept.
+ *   MX materialize  out = BF16_rne(decode(code) * 2^(e-127)) (the product is exact).
+ * Inputs must be finite; results for NaN or infinity inputs are not specified.
+ *
+ * Conventions shared by every call:
+ *   - All data pointers are DEVICE pointers owned by the caller (host arrays of
+ *     device pointers where stated). The library allocates nothing, keeps no state
+ *     between calls beyond a per-device cache of launch parameters, and never
+ *     synchronizes: work is enqueued on `stream` (0 = the legacy default stream)
+ *     and the call returns.
+ *   - Every check happens before any launch; a call that returns an error has not
+ *     touched device memory. n == 0 (or rows == 0 / cols == 0) is a valid no-op and
+ *     returns BQ_OK without launching.
+ *   - Shape: n % 128 == 0 and, for MX, cols % 128 == 0 — otherwise BQ_ERR_SHAPE and
+ *     the caller keeps its BF16 path ("feat(pcie_dma): add INT8 and MXFP8 wire
+ *     modes", Configuration: compressed transport needs a shard divisible by 128).
+ *   - Alignment: BF16 and payload/value pointers 16-byte aligned; INT8 scale pointers
+ *     4-byte aligned; MX scale pointers 4-byte aligned with ld_s % 4 == 0; MX strides
+ *     keep every row 16-byte aligned (ld_x % 8 == 0 elements, ld_q % 16 == 0 bytes,
+ *     ld_out % 8 == 0 elements). Otherwise BQ_ERR_ALIGN.
+ *   - Outputs may not overlap inputs or each other (checked on the address ranges
+ *     the call touches; strided MX ranges are taken as their bounding intervals).
+ *     Otherwise BQ_ERR_ALIAS.
+ *   - A failed kernel launch returns BQ_ERR_CUDA (the CUDA error is left readable
+ *     through cudaGetLastError's usual rules only as far as this call consumed it).
+ *   - Errors in earlier asynchronous work on the stream are not detected here.
+ */
+#ifndef BQ_H
+#define BQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define BQ_API __attribute__((visibility("default")))
+#else
+#define BQ_API
+#endif
+
+#define BQ_ABI_VERSION 1
+#define BQ_BLOCK_I8 128 /* values per INT8 block */
+#define BQ_GROUP_MX 32  /* values per E8M0 scale */
+#define BQ_MAX_W 16     /* most sources one accumulate call takes */
+
+typedef enum {
+    BQ_OK = 0,
+    BQ_ERR_NULL = 1,  /* a required pointer is NULL */
+    BQ_ERR_SHAPE = 2, /* n or cols not a multiple of 128, negative size, W out of
+                         [1, BQ_MAX_W], or a leading dimension too small */
+    BQ_ERR_ALIGN = 3, /* a pointer or leading dimension breaks the alignment rules */
+    BQ_ERR_ALIAS = 4, /* an output overlaps an input or another output */
+    BQ_ERR_CUDA = 5   /* the CUDA runtime reported an error for this call's launch */
+} bq_status;
+
+/* BQ_ABI_VERSION of the loaded library. */
+BQ_API int bq_abi_version(void);
+
+/* Static English description of a status code (never NULL). */
+BQ_API const char *bq_status_string(int status);
+
+/* Bytes on the wire for n values in either codec: 132 * n / 128 ("feat(pcie_dma):
+ * add block-INT8 wire modes for AG, ring, and A2A", Summary). Returns -1 when
+ * n < 0 or n % 128 != 0. */
+BQ_API int64_t bq_wire_bytes(int64_t n);
+
+/* BF16 -> block INT8 ("feat(pcie_dma): add block-INT8 wire modes for AG, ring, and
+ * A2A", Implementation: BF16 -> signed INT8 quantization, one scale per 128 values).
+ *   x_bf16   [n] BF16, 16-byte aligned (read)
+ *   q        [n] int8 payload, 16-byte aligned (written)
+ *   scales   [n/128] FP32, 4-byte aligned (written) */
+BQ_API bq_status bq_quant_i8(const void *x_bf16, int64_t n, int8_t *q, float *scales,
+                      cudaStream_t stream);
+
+/* Block INT8 -> BF16 materialization (same page, Implementation: signed INT8 -> BF16
+ * materialization; Summary: owners materialize from the forwarded payload).
+ *   q [n] int8 (read), scales [n/128] FP32 (read), out_bf16 [n] BF16 (written). */
+BQ_API bq_status bq_dequant_i8(const int8_t *q, const float *scales, int64_t n, void *out_bf16,
+                        cudaStream_t stream);
+
+/* Multi-source dequantize with FP32 accumulation, then requantize (same page,
+ * Implementation: multi-source INT8 dequantization with FP32 accumulation for A2A).
+ *   q_srcs, scale_srcs  HOST arrays of W DEVICE pointers ([n] int8 and [n/128] FP32
+ *                       each); their order is the summation order
+ *   W                   1 <= W <= BQ_MAX_W
+ *   q_out, scales_out   the requantized payload (written)
+ *   out_bf16            NULL, or [n] BF16 receiving the materialization of the new
+ *                       payload, bit-identical to bq_dequant_i8(q_out, scales_out)
+ *                       (the owner materializes the payload it forwards).
+ * Sources may repeat or overlap one another. */
+BQ_API bq_status bq_dequant_accum_i8(const int8_t *const *q_srcs, const float *const *scale_srcs,
+                              int W, int64_t n, int8_t *q_out, float *scales_out,
+                              void *out_bf16, cudaStream_t stream);
+
+/* Fused ring reduce-scatter hop: dequantize the incoming payload, add the local BF16
+ * shard in FP32, requantize (same page, Implementation: fused INT8
+ * dequantize-add-requantize for each ring reduce-scatter hop).
+ *   q_in [n], s_in [n/128]   incoming payload (read)
+ *   x_local_bf16 [n]         this rank's shard (read)
+ *   q_out, s_out             outgoing payload (written)
+ *   out_bf16                 NULL, or [n] BF16 materialization of the outgoing
+ *                            payload (for the hop that ends at the owner). */
+BQ_API bq_status bq_ring_hop_i8(const int8_t *q_in, const float *s_in, const void *x_local_bf16,
+                         int64_t n, int8_t *q_out, float *s_out, void *out_bf16,
+                         cudaStream_t stream);
+
+/* BF16 [rows, cols] -> MXFP8 ("feat(pcie_dma): add INT8 and MXFP8 wire modes",
+ * Summary and the mxfp8_scale_byte review comment). Row-major with leading
+ * dimensions, so a 128-column-aligned slice of a wider buffer is addressed by
+ * offsetting the pointers: q_e4m3 + col0 and s_e8m0 + col0/32 with col0 % 128 == 0
+ * ("[II] Support staged MXFP8 linear inputs", Behavior and Compatibility).
+ *   x_bf16  [rows][ld_x] BF16 (read);      ld_x >= cols, ld_x % 8 == 0
+ *   q_e4m3  [rows][ld_q] bytes (written);  ld_q >= cols, ld_q % 16 == 0
+ *   s_e8m0  [rows][ld_s] bytes (written);  ld_s >= cols/32, ld_s % 4 == 0 */
+BQ_API bq_status bq_quant_mx(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld_x,
+                      uint8_t *q_e4m3, int64_t ld_q, uint8_t *s_e8m0, int64_t ld_s,
+                      cudaStream_t stream);
+
+/* MXFP8 -> BF16 materialization (same page, review: dma_dequant_store_mx).
+ *   q_e4m3 [rows][ld_q], s_e8m0 [rows][ld_s] (read); out_bf16 [rows][ld_out] (written),
+ *   ld_out >= cols, ld_out % 8 == 0. Scale byte 255 and codes 0x7F/0xFF are NaN. */
+BQ_API bq_status bq_dequant_mx(const uint8_t *q_e4m3, int64_t ld_q, const uint8_t *s_e8m0,
+                        int64_t ld_s, int64_t rows, int64_t cols, void *out_bf16,
+                        int64_t ld_out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BQ_H */

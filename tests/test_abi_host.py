@@ -1,0 +1,147 @@
+"""The C ABI without a GPU: libbq.so loads, exports every entry point include/bq.h
+declares, and rejects invalid arguments before any CUDA call.
+
+Every call here carries at least one invalid argument, so the library returns an error
+status before it would touch the device; the fake pointers are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bq.h")
+
+OK, NULL, SHAPE, ALIGN, ALIAS, CUDA = range(6)
+A = 0x7F0000000000  # a 256-byte-aligned fake device address, never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"BQ_API\s+[\w\s\*]*?\b(bq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for want in ("bq_quant_i8", "bq_dequant_i8", "bq_dequant_accum_i8", "bq_ring_hop_i8", "bq_quant_mx",
+                 "bq_dequant_mx", "bq_wire_bytes", "bq_status_string", "bq_abi_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(bq_lib):
+    for name in declared_functions():
+        assert hasattr(bq_lib, name), name
+    assert bq_lib.bq_abi_version() == 1
+
+
+def test_wire_bytes_and_status_strings(bq_lib):
+    assert bq_lib.bq_wire_bytes(0) == 0
+    assert bq_lib.bq_wire_bytes(128) == 132
+    assert bq_lib.bq_wire_bytes(512 * 7168) == 3784704
+    assert bq_lib.bq_wire_bytes(65536 * 7168) == 484442112
+    assert bq_lib.bq_wire_bytes(100) == -1
+    assert bq_lib.bq_wire_bytes(-128) == -1
+    for s in range(6):
+        assert bq_lib.bq_status_string(s)
+    assert bq_lib.bq_status_string(99) == b"unknown status"
+
+
+def _srcs(ptrs):
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def test_quant_i8_rejections(bq_lib):
+    f = bq_lib.bq_quant_i8
+    n = 1024
+    assert f(A, 100, A + 0x100000, A + 0x200000, None) == SHAPE
+    assert f(A, -128, A + 0x100000, A + 0x200000, None) == SHAPE
+    assert f(None, 0, None, None, None) == OK  # empty input: nothing to do, no launch
+    assert f(None, n, A + 0x100000, A + 0x200000, None) == NULL
+    assert f(A, n, None, A + 0x200000, None) == NULL
+    assert f(A, n, A + 0x100000, None, None) == NULL
+    assert f(A + 8, n, A + 0x100000, A + 0x200000, None) == ALIGN
+    assert f(A, n, A + 0x100004, A + 0x200000, None) == ALIGN
+    assert f(A, n, A + 0x100000, A + 0x200002, None) == ALIGN
+    assert f(A, n, A + 1024, A + 0x200000, None) == ALIAS  # payload inside x (x spans 2n bytes)
+    assert f(A, n, A + 0x100000, A + 0x100000 + n - 4, None) == ALIAS  # scales overlap payload
+
+
+def test_dequant_i8_rejections(bq_lib):
+    f = bq_lib.bq_dequant_i8
+    n = 2048
+    assert f(A, A + 0x100000, 129, A + 0x200000, None) == SHAPE
+    assert f(A, A + 0x100000, 0, None, None) == OK
+    assert f(A, None, n, A + 0x200000, None) == NULL
+    assert f(A, A + 0x100000, n, A + 0x200008, None) == ALIGN
+    assert f(A, A + 0x100000, n, A + 0x100000 - 64, None) == ALIAS
+
+
+def test_accum_i8_rejections(bq_lib):
+    f = bq_lib.bq_dequant_accum_i8
+    n = 4096
+    q = [A + k * 0x100000 for k in range(4)]
+    s = [A + 0x1000000 + k * 0x10000 for k in range(4)]
+    qp, qa = _srcs(q)
+    sp, sa = _srcs(s)
+    out_q, out_s, out_b = A + 0x2000000, A + 0x3000000, A + 0x4000000
+    assert f(qp, sp, 0, n, out_q, out_s, None, None) == SHAPE
+    assert f(qp, sp, 17, n, out_q, out_s, None, None) == SHAPE
+    assert f(qp, sp, 4, n + 64, out_q, out_s, None, None) == SHAPE
+    assert f(qp, sp, 4, 0, out_q, out_s, None, None) == OK
+    assert f(None, sp, 4, n, out_q, out_s, None, None) == NULL
+    qn, qna = _srcs([q[0], None, q[2], q[3]])
+    assert f(qn, sp, 4, n, out_q, out_s, None, None) == NULL
+    qm, qma = _srcs([q[0], q[1] + 4, q[2], q[3]])
+    assert f(qm, sp, 4, n, out_q, out_s, None, None) == ALIGN
+    assert f(qp, sp, 4, n, out_q, out_s, out_b + 2, None) == ALIGN
+    assert f(qp, sp, 4, n, q[2], out_s, None, None) == ALIAS  # output payload is a source
+    assert f(qp, sp, 4, n, out_q, s[3] + 16, None, None) == ALIAS
+    assert f(qp, sp, 4, n, out_q, out_s, out_q + 1024, None) == ALIAS  # BF16 out over payload out
+
+
+def test_ring_hop_rejections(bq_lib):
+    f = bq_lib.bq_ring_hop_i8
+    n = 4096
+    qi, si, x, qo, so, ob = (A + k * 0x100000 for k in range(6))
+    assert f(qi, si, x, 96, qo, so, None, None) == SHAPE
+    assert f(qi, si, x, 0, qo, so, None, None) == OK
+    assert f(qi, si, None, n, qo, so, None, None) == NULL
+    assert f(qi, si + 2, x, n, qo, so, None, None) == ALIGN
+    assert f(qi, si, x, n, x + 16, so, None, None) == ALIAS
+    assert f(qi, si, x, n, qo, so, qi, None) == ALIAS
+
+
+def test_mx_rejections(bq_lib):
+    fq = bq_lib.bq_quant_mx
+    fd = bq_lib.bq_dequant_mx
+    x, q, s, o = A, A + 0x1000000, A + 0x2000000, A + 0x3000000
+    rows, cols = 64, 256
+    assert fq(x, rows, 200, 256, q, 256, s, 8, None) == SHAPE  # cols % 128
+    assert fq(x, -1, cols, cols, q, cols, s, 8, None) == SHAPE
+    assert fq(x, 0, cols, cols, q, cols, s, 8, None) == OK
+    assert fq(x, rows, cols, 128, q, cols, s, 8, None) == SHAPE  # ld_x < cols
+    assert fq(x, rows, cols, cols, q, cols, s, 4, None) == SHAPE  # ld_s < cols/32
+    assert fq(None, rows, cols, cols, q, cols, s, 8, None) == NULL
+    assert fq(x, rows, cols, cols + 4, q, cols, s, 8, None) == ALIGN  # ld_x % 8
+    assert fq(x, rows, cols, cols, q, cols + 8, s, 8, None) == ALIGN  # ld_q % 16
+    assert fq(x, rows, cols, cols, q, cols, s + 2, 8, None) == ALIGN  # s 4-byte aligned
+    assert fq(x, rows, cols, cols, q, cols, s, 10, None) == ALIGN  # ld_s % 4
+    assert fq(x, rows, cols, cols, x + 2 * cols * (rows - 1), cols, s, 8, None) == ALIAS
+    assert fq(x, rows, cols, cols, q, cols, q + cols * rows - 4, 8, None) == ALIAS
+    assert fd(q, cols, s, 8, rows, 100, o, cols, None) == SHAPE
+    assert fd(q, cols, s, 8, 0, cols, o, cols, None) == OK
+    assert fd(q, cols, s, 8, rows, cols, None, cols, None) == NULL
+    assert fd(q, cols, s, 8, rows, cols, o, cols + 2, None) == ALIGN
+    assert fd(q, cols, s, 8, rows, cols, q - 2 * cols, cols, None) == ALIAS
+
+
+def test_binding_without_library_fails_loudly(tmp_path, monkeypatch):
+    # the binding never falls back: a missing library raises instead of computing
+    from block_quantized_wire_gb300 import _lib, build
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing_libbq.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.load()
