@@ -21,7 +21,6 @@ namespace bqk {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSegs = 4;                      // segments per warp iteration
 constexpr int kChunkBlocks = 2 * kSegs;       // 128-value blocks per warp iteration
-constexpr float kFltMin = 1.17549435e-38f;    // smallest normal binary32
 
 // ---------------------------------------------------------------- global memory
 // Inputs are read once: non-coherent path, no L1 allocation.
@@ -116,64 +115,60 @@ __device__ __forceinline__ void i8x8_to_f32(uint2 w, float (&v)[8])
 }
 
 // ---------------------------------------------------------------- block INT8 scale
-// s = fl(amax / 127). For a normal s the quotients x/s are formed as x * fl(1/s) and
-// checked (see i8_quant8); a subnormal s (tiny FP32 sums only) takes the exact path
-// for the whole block; s == 0 gives payload 0 (r = 0 makes every t zero).
-struct I8Scale {
-    float s;
-    float r;
-    bool exact_only;
-};
+// s = fl(amax / 127) and r = fl(1 / s), both IEEE round-to-nearest, computed once per
+// block. A block with s < 2^-100 (amax below about 1e-28: tiny FP32 sums or tiny BF16
+// inputs) is flagged by r = -1 and quantized with the IEEE division x / s, because
+// there the remainders of i8_quotient could fall into the subnormal range and lose
+// bits; s == 0 gives r = 0, for which the quotient below is 0 and the payload 0.
+constexpr float kQuotientMinScale = 7.88860905e-31f;  // 2^-100
 
-__device__ __forceinline__ I8Scale i8_scale(float amax)
+__device__ __forceinline__ void i8_block_scale(float amax, float &s, float &r)
 {
-    I8Scale b;
-    b.s = __fdiv_rn(amax, 127.0f);
-    const bool normal = b.s >= kFltMin;
-    b.r = normal ? __frcp_rn(b.s) : 0.0f;
-    b.exact_only = (b.s > 0.0f) && !normal;
-    return b;
+    s = __fdiv_rn(amax, 127.0f);
+    r = s >= kQuotientMinScale ? __frcp_rn(s) : (s > 0.0f ? -1.0f : 0.0f);
 }
 
-// Quantize eight values of one block. Returns the payload bytes (value i in byte i)
-// and leaves the integers, as binary32 (+0 for zero), in qf for a fused
-// materialization.
-//
-// Fast path (s normal): t = fl(x * fl(1/s)) differs from x/s by less than 2^-15 (|x/s|
-// <= 127.00002, two roundings of relative 2^-24 each), and fl(x/s) differs from x/s
-// by at most 2^-18, so |t - fl(x/s)| < 2^-14. When t is farther than 2^-14 from every
-// half-integer, t and fl(x/s) round to the same integer; adding 1.5 * 2^23 performs
-// that rounding (ties to even) and leaves the integer in the low mantissa bits, whose
-// low byte is the two's-complement payload byte. Otherwise (about 1 value in 8000)
-// the lane recomputes its eight values with the IEEE division x / s.
-__device__ __forceinline__ uint2 i8_quant8(const float (&v)[8], const I8Scale &b, float (&qf)[8])
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+
+// fl(x / s) for a normal s with r = fl(1 / s), by Markstein's correction (P. W.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990): when q is within one ulp of x/s and
+// r is the correctly rounded reciprocal, the remainder x - q*s is exact (one FMA) and
+// fl(q + (x - q*s) * r) is the correctly rounded quotient. t0 = fl(x * r) is only
+// known to be within 1.5 ulp, so one correction brings it within an ulp and a second
+// one rounds correctly. |x / s| <= 127.0001 here, so nothing overflows. With s >=
+// 2^-100, a remainder of a quotient >= 1/4 is a multiple of ulp(t) * ulp(s) >= 2^-149
+// and so representable even when subnormal; quotients below 1/4 round to payload 0
+// whatever their last bits.
+__device__ __forceinline__ float i8_quotient(float x, float s, float r)
 {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    constexpr float kNearHalf = 0.49993896484375f;  // 1/2 - 2^-14
-    uint32_t w[8];
-    float dmax = 0.0f;
+    const float t0 = __fmul_rn(x, r);
+    const float t1 = __fmaf_rn(__fmaf_rn(-t0, s, x), r, t0);
+    return __fmaf_rn(__fmaf_rn(-t1, s, x), r, t1);
+}
+
+// Quantize eight values of one block with scale s and reciprocal r (i8_block_scale).
+// Returns, per value, the binary32 word M + k (M = 1.5 * 2^23, k the payload integer):
+// adding M to the quotient rounds it to the nearest integer, ties to even, and leaves
+// k in the low mantissa bits, so the word's low byte is k in two's complement and
+// k = word - M exactly. |fl(x/s)| <= fl(amax/s) < 127.5 for a normal s, so no clamp
+// is needed there; the subnormal-s path clamps to [-127, 127].
+__device__ __forceinline__ void i8_quant8(const float (&v)[8], float s, float r, uint32_t (&w)[8])
+{
+    if (__builtin_expect(r >= 0.0f, 1)) {
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const float t = __fmul_rn(v[i], b.r);
-        const float y = __fadd_rn(t, kMagic);
-        const float k = __fsub_rn(y, kMagic);
-        dmax = fmaxf(dmax, fabsf(__fsub_rn(t, k)));
-        w[i] = __float_as_uint(y);
-        qf[i] = k;
-    }
-    if (dmax > kNearHalf || b.exact_only) {
+        for (int i = 0; i < 8; i++) w[i] = __float_as_uint(__fadd_rn(i8_quotient(v[i], s, r), kMagic));
+    } else {
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            float k = 0.0f;
-            if (b.s != 0.0f) {
-                k = rintf(__fdiv_rn(v[i], b.s));
-                k = fminf(fmaxf(k, -127.0f), 127.0f);
-            }
-            const float y = __fadd_rn(k, kMagic);
-            w[i] = __float_as_uint(y);
-            qf[i] = __fsub_rn(y, kMagic);  // canonical: -0 becomes +0
+            const float k = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -127.0f), 127.0f);
+            w[i] = __float_as_uint(__fadd_rn(k, kMagic));
         }
     }
+}
+
+__device__ __forceinline__ uint2 pack_payload8(const uint32_t (&w)[8])
+{
     return make_uint2(pack_low_bytes(w[0], w[1], w[2], w[3]), pack_low_bytes(w[4], w[5], w[6], w[7]));
 }
 
@@ -195,7 +190,16 @@ __device__ __forceinline__ float halfwarp_max(float m)
     return m;
 }
 
-// BF16 of fl(q * s) for eight integers held as binary32.
+// BF16 of fl(k * s) for the eight payload integers held as words M + k.
+__device__ __forceinline__ uint4 i8_materialize_words(const uint32_t (&w)[8], float s)
+{
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) d[i] = __fmul_rn(__fsub_rn(__uint_as_float(w[i]), kMagic), s);
+    return f32x8_to_bf16x8(d);
+}
+
+// BF16 of fl(q * s) for eight payload integers held as binary32.
 __device__ __forceinline__ uint4 i8_materialize8(const float (&qf)[8], float s)
 {
     float d[8];

@@ -2,237 +2,406 @@
 //
 // Operations from "feat(pcie_dma): add block-INT8 wire modes for AG, ring, and A2A",
 // Implementation (the four kernels) and Summary (128 values per block, one FP32
-// scale = amax/127, owners materialize the forwarded payload). The decomposition into
-// warp chunks and segments is described in bq_device.cuh.
+// scale = amax/127, owners materialize the forwarded payload).
+//
+// Decomposition (see bq_device.cuh): a warp processes a chunk of SEGS segments of 256
+// values; in segment j lane l holds values [256j + 8l, 256j + 8l + 8) of the chunk, so
+// half-warp h holds block 2j + h. Per chunk, the block amaxes are gathered into lanes
+// 0..2*SEGS-1, which compute the chunk's scales once; the scales are then broadcast
+// back per segment and stored by those lanes in one coalesced store. Full chunks run
+// without bounds checks; the one partial chunk at the end (n not a multiple of the
+// chunk) runs the same code with checks.
 #include "bq_device.cuh"
 #include "bq_launch.h"
 
 namespace bqk {
 namespace {
 
-__device__ __forceinline__ int64_t first_chunk() { return (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); }
-__device__ __forceinline__ int64_t chunk_stride() { return (int64_t)gridDim.x * (kThreads / 32); }
+__device__ __forceinline__ int64_t warp_id() { return ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; }
+__device__ __forceinline__ int64_t warp_count() { return ((int64_t)gridDim.x * kThreads) >> 5; }
 
-// Hand the scale of segment j (held by every lane of each half-warp) to lane 2j+h, so
-// that after the chunk lanes 0..kChunkBlocks-1 hold the chunk's scales in block order.
-__device__ __forceinline__ void collect_scale(float s_seg, int j, int lane, float &mine)
+// Lane-held amax of each segment -> lane 2j+h holds block (2j+h)'s amax.
+template <int SEGS>
+__device__ __forceinline__ float gather_amax(const float (&m)[SEGS], int lane)
 {
-    const float lo = __shfl_sync(kFull, s_seg, 0);
-    const float hi = __shfl_sync(kFull, s_seg, 16);
-    if (lane == 2 * j) mine = lo;
-    if (lane == 2 * j + 1) mine = hi;
-}
-
-// Requantize one segment (8 FP32 values per lane), store its payload and, when kOut,
-// its BF16 materialization; returns the block scale.
-template <bool kOut>
-__device__ __forceinline__ float requant_segment(const float (&v)[8], int64_t elem, bool valid,
-                                                 int8_t *__restrict__ q, uint16_t *__restrict__ out)
-{
-    const I8Scale sc = i8_scale(halfwarp_max(amax8(v)));
-    float qf[8];
-    const uint2 packed = i8_quant8(v, sc, qf);
-    if (valid) {
-        st_v2(q + elem, packed);
-        if (kOut) st_v4(out + elem, i8_materialize8(qf, sc.s));
+    float mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) {
+        const float g = __shfl_sync(kFull, m[j], (lane & 1) << 4);
+        if ((lane >> 1) == j) mine = g;
     }
-    return sc.s;
+    return mine;
 }
 
+// Requantize SEGS segments of FP32 values (v[j] = lane's 8 values of segment j):
+// writes the payload, the chunk's scales and, when kOut, the BF16 materialization.
+template <int SEGS, bool kTail, bool kOut>
+__device__ __forceinline__ void requant_chunk(const float (&v)[SEGS][8], int64_t e0, int64_t b0, int64_t nblk,
+                                              int lane, int8_t *__restrict__ q, float *__restrict__ s,
+                                              uint16_t *__restrict__ out)
+{
+    const int half = lane >> 4;
+    float m[SEGS];
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) m[j] = halfwarp_max(amax8(v[j]));
+    float sc, rc;
+    i8_block_scale(gather_amax<SEGS>(m, lane), sc, rc);
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) {
+        const float sj = __shfl_sync(kFull, sc, 2 * j + half);
+        const float rj = __shfl_sync(kFull, rc, 2 * j + half);
+        uint32_t w[8];
+        i8_quant8(v[j], sj, rj, w);
+        if (!kTail || b0 + 2 * j + half < nblk) {
+            st_v2(q + e0 + 256 * j, pack_payload8(w));
+            if (kOut) st_v4(out + e0 + 256 * j, i8_materialize_words(w, sj));
+        }
+    }
+    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) s[b0 + lane] = sc;
+}
+
+// Grid-stride driver over warp chunks. With kPrefetch, the loads of a warp's next
+// chunk (c + number of warps) are issued before chunk c is computed (a register
+// pipeline; it pays only where registers are cheap, as in materialize). Op provides
+//   In                                 registers holding one chunk's inputs
+//   load<kTail>(In&, c) / compute<kTail>(const In&, c)
+// Full chunks use kTail = false (no bounds checks); the one partial chunk, if any,
+// is loaded and computed by the warp whose stride lands on it.
+template <bool kPrefetch, class Op>
+__device__ __forceinline__ void run_chunks(const Op &op, int64_t nblk, int chunk_blocks)
+{
+    const int64_t nfull = nblk / chunk_blocks;
+    const int64_t stride = warp_count();
+    int64_t c = warp_id();
+    if (!kPrefetch) {
+        for (; c < nfull; c += stride) {
+            typename Op::In cur;
+            op.template load<false>(cur, c);
+            op.template compute<false>(cur, c);
+        }
+    } else if (c < nfull) {
+        typename Op::In cur;
+        op.template load<false>(cur, c);
+        while (true) {
+            const int64_t nc = c + stride;
+            const bool more = nc < nfull;
+            typename Op::In nxt;
+            if (more) op.template load<false>(nxt, nc);
+            op.template compute<false>(cur, c);
+            c = nc;
+            if (!more) break;
+            cur = nxt;
+        }
+    }
+    if (c == nfull && nblk % chunk_blocks) {
+        typename Op::In t;
+        op.template load<true>(t, c);
+        op.template compute<true>(t, c);
+    }
+}
+
+// ---------------------------------------------------------------- quantize
+template <int SEGS>
+struct QuantOp {
+    const uint16_t *__restrict__ x;
+    int8_t *__restrict__ q;
+    float *__restrict__ s;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint4 x[SEGS];
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+#pragma unroll
+        for (int j = 0; j < SEGS; j++)
+            in.x[j] = (!kTail || b0 + 2 * j + (lane >> 4) < nblk) ? ld_stream_v4(x + e0 + 256 * j)
+                                                                  : make_uint4(0, 0, 0, 0);
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float v[SEGS][8];
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
+        requant_chunk<SEGS, kTail, false>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, nullptr);
+    }
+};
+
+template <int SEGS>
 __global__ void __launch_bounds__(kThreads)
 quant_i8_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int64_t nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-    for (int64_t c = first_chunk(); c < nchunk; c += chunk_stride()) {
-        const int64_t b0 = c * kChunkBlocks;
-        uint4 raw[kSegs];
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            raw[j] = blk < nblk ? ld_stream_v4(x + blk * 128 + hl * 8) : make_uint4(0, 0, 0, 0);
-        }
-        float mine = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            float v[8];
-            bf16x8_to_f32(raw[j], v);
-            const float sj = requant_segment<false>(v, blk * 128 + hl * 8, blk < nblk, q, nullptr);
-            collect_scale(sj, j, lane, mine);
-        }
-        if (lane < kChunkBlocks && b0 + lane < nblk) s[b0 + lane] = mine;
-    }
+    const QuantOp<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
+// ---------------------------------------------------------------- materialize
+template <int SEGS>
+struct DequantOp {
+    const int8_t *__restrict__ q;
+    const float *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint2 q[SEGS];
+        float sc;
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+#pragma unroll
+        for (int j = 0; j < SEGS; j++)
+            in.q[j] = (!kTail || b0 + 2 * j + (lane >> 4) < nblk) ? ld_stream_v2(q + e0 + 256 * j) : make_uint2(0, 0);
+        in.sc = (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) ? __uint_as_float(ld_stream_u32(s + b0 + lane))
+                                                                   : 0.0f;
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+        const int half = lane >> 4;
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            const float sj = __shfl_sync(kFull, in.sc, 2 * j + half);
+            float v[8];
+            i8x8_to_f32(in.q[j], v);
+            if (!kTail || b0 + 2 * j + half < nblk) st_v4(out + e0 + 256 * j, i8_materialize8(v, sj));
+        }
+    }
+};
+
+template <int SEGS>
 __global__ void __launch_bounds__(kThreads)
-dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk,
-                  uint16_t *__restrict__ out)
+dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk, uint16_t *__restrict__ out)
 {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int64_t nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-    for (int64_t c = first_chunk(); c < nchunk; c += chunk_stride()) {
-        const int64_t b0 = c * kChunkBlocks;
-        uint2 raw[kSegs];
+    const DequantOp<SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<true>(op, nblk, 2 * SEGS);
+}
+
+// ---------------------------------------------------------------- accumulate
+// Sources are summed in source order 0..nsrc-1. The first W sources of a chunk are
+// loaded together (and prefetched by the pipeline); any further sources are loaded
+// in groups of W with the running sum carried in registers.
+template <int SEGS, int W>
+struct SourceRegs {
+    uint2 q[W][SEGS];
+    float sc[W];
+};
+
+template <int SEGS, int W, bool kTail>
+__device__ __forceinline__ void load_sources(SourceRegs<SEGS, W> &r, const SourceList &src, int g, int nsrc,
+                                             int64_t c, int64_t nblk, int lane)
+{
+    const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+    const bool lane_ok = lane < 2 * SEGS && (!kTail || b0 + lane < nblk);
 #pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            raw[j] = blk < nblk ? ld_stream_v2(q + blk * 128 + hl * 8) : make_uint2(0, 0);
-        }
-        const float sc =
-            (lane < kChunkBlocks && b0 + lane < nblk) ? __uint_as_float(ld_stream_u32(s + b0 + lane)) : 0.0f;
+    for (int i = 0; i < W; i++) {
+        const bool src_ok = g + i < nsrc;
+        const int8_t *qw = src.q[src_ok ? g + i : g];
+        const float *sw = src.s[src_ok ? g + i : g];
 #pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            const float sj = __shfl_sync(kFull, sc, 2 * j + half);
+        for (int j = 0; j < SEGS; j++)
+            r.q[i][j] = (src_ok && (!kTail || b0 + 2 * j + (lane >> 4) < nblk)) ? ld_stream_v2(qw + e0 + 256 * j)
+                                                                                 : make_uint2(0, 0);
+        r.sc[i] = (src_ok && lane_ok) ? __uint_as_float(ld_stream_u32(sw + b0 + lane)) : 0.0f;
+    }
+}
+
+template <int SEGS, int W, bool kFirst>
+__device__ __forceinline__ void add_sources(const SourceRegs<SEGS, W> &r, int g, int nsrc, float (&acc)[SEGS][8],
+                                            int lane)
+{
+    const int half = lane >> 4;
+#pragma unroll
+    for (int i = 0; i < W; i++) {
+        if (g + i >= nsrc) break;
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            const float sj = __shfl_sync(kFull, r.sc[i], 2 * j + half);
             float v[8];
-            i8x8_to_f32(raw[j], v);
-            if (blk < nblk) st_v4(out + blk * 128 + hl * 8, i8_materialize8(v, sj));
+            i8x8_to_f32(r.q[i][j], v);
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const float d = __fmul_rn(v[e], sj);
+                acc[j][e] = (kFirst && i == 0) ? d : __fadd_rn(acc[j][e], d);
+            }
         }
     }
 }
 
-// Sources are consumed in groups of four so that each group's loads are in flight
-// together; the running sum is carried across groups in source order.
-template <bool kOut>
+template <int SEGS, int W, bool kOut>
+struct AccumOp {
+    const SourceList &src;  // the kernel's __grid_constant__ parameter, read in place
+    int nsrc;
+    int8_t *__restrict__ q;
+    float *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    using In = SourceRegs<SEGS, W>;
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        load_sources<SEGS, W, kTail>(in, src, 0, nsrc, c, nblk, lane);
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float acc[SEGS][8];
+        add_sources<SEGS, W, true>(in, 0, nsrc, acc, lane);
+        for (int g = W; g < nsrc; g += W) {
+            In more;
+            load_sources<SEGS, W, kTail>(more, src, g, nsrc, c, nblk, lane);
+            add_sources<SEGS, W, false>(more, g, nsrc, acc, lane);
+        }
+        requant_chunk<SEGS, kTail, kOut>(acc, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, out);
+    }
+};
+
+template <int SEGS, int W, bool kOut>
 __global__ void __launch_bounds__(kThreads)
-accum_i8_kernel(const SourceList src, int W, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s,
+accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s,
                 uint16_t *__restrict__ out)
 {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int64_t nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-    for (int64_t c = first_chunk(); c < nchunk; c += chunk_stride()) {
-        const int64_t b0 = c * kChunkBlocks;
-        const bool lane_blk_ok = lane < kChunkBlocks && b0 + lane < nblk;
-        float acc[kSegs][8];
-        for (int w0 = 0; w0 < W; w0 += 4) {
-            uint2 raw[4][kSegs];
-            float sc[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                if (w0 + i < W) {
-                    const int8_t *qw = src.q[w0 + i];
-#pragma unroll
-                    for (int j = 0; j < kSegs; j++) {
-                        const int64_t blk = b0 + 2 * j + half;
-                        raw[i][j] = blk < nblk ? ld_stream_v2(qw + blk * 128 + hl * 8) : make_uint2(0, 0);
-                    }
-                    sc[i] = lane_blk_ok ? __uint_as_float(ld_stream_u32(src.s[w0 + i] + b0 + lane)) : 0.0f;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                if (w0 + i < W) {
-#pragma unroll
-                    for (int j = 0; j < kSegs; j++) {
-                        const float sj = __shfl_sync(kFull, sc[i], 2 * j + half);
-                        float v[8];
-                        i8x8_to_f32(raw[i][j], v);
-                        if (w0 + i == 0) {
-#pragma unroll
-                            for (int e = 0; e < 8; e++) acc[j][e] = __fmul_rn(v[e], sj);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; e++) acc[j][e] = __fadd_rn(acc[j][e], __fmul_rn(v[e], sj));
-                        }
-                    }
-                }
-            }
-        }
-        float mine = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            const float sj = requant_segment<kOut>(acc[j], blk * 128 + hl * 8, blk < nblk, q, out);
-            collect_scale(sj, j, lane, mine);
-        }
-        if (lane_blk_ok) s[b0 + lane] = mine;
-    }
+    const AccumOp<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
-template <bool kOut>
+// ---------------------------------------------------------------- ring hop
+template <int SEGS, bool kOut>
+struct HopOp {
+    const int8_t *__restrict__ q_in;
+    const float *__restrict__ s_in;
+    const uint16_t *__restrict__ x;
+    int8_t *__restrict__ q;
+    float *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint2 q[SEGS];
+        uint4 x[SEGS];
+        float sc;
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            const bool ok = !kTail || b0 + 2 * j + (lane >> 4) < nblk;
+            in.q[j] = ok ? ld_stream_v2(q_in + e0 + 256 * j) : make_uint2(0, 0);
+            in.x[j] = ok ? ld_stream_v4(x + e0 + 256 * j) : make_uint4(0, 0, 0, 0);
+        }
+        in.sc = (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) ? __uint_as_float(ld_stream_u32(s_in + b0 + lane))
+                                                                   : 0.0f;
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        const int half = lane >> 4;
+        float v[SEGS][8];
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            const float sj = __shfl_sync(kFull, in.sc, 2 * j + half);
+            float d[8], xl[8];
+            i8x8_to_f32(in.q[j], d);
+            bf16x8_to_f32(in.x[j], xl);
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[j][e] = __fadd_rn(__fmul_rn(d[e], sj), xl[e]);
+        }
+        requant_chunk<SEGS, kTail, kOut>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, out);
+    }
+};
+
+template <int SEGS, bool kOut>
 __global__ void __launch_bounds__(kThreads)
-ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_in,
-                   const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q,
-                   float *__restrict__ s, uint16_t *__restrict__ out)
+ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_in, const uint16_t *__restrict__ x,
+                   int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s, uint16_t *__restrict__ out)
 {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int64_t nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-    for (int64_t c = first_chunk(); c < nchunk; c += chunk_stride()) {
-        const int64_t b0 = c * kChunkBlocks;
-        const bool lane_blk_ok = lane < kChunkBlocks && b0 + lane < nblk;
-        uint2 rq[kSegs];
-        uint4 rx[kSegs];
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            const bool ok = blk < nblk;
-            rq[j] = ok ? ld_stream_v2(q_in + blk * 128 + hl * 8) : make_uint2(0, 0);
-            rx[j] = ok ? ld_stream_v4(x + blk * 128 + hl * 8) : make_uint4(0, 0, 0, 0);
-        }
-        const float sc = lane_blk_ok ? __uint_as_float(ld_stream_u32(s_in + b0 + lane)) : 0.0f;
-        float mine = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            const int64_t blk = b0 + 2 * j + half;
-            const float sj = __shfl_sync(kFull, sc, 2 * j + half);
-            float d[8], xl[8], v[8];
-            i8x8_to_f32(rq[j], d);
-            bf16x8_to_f32(rx[j], xl);
-#pragma unroll
-            for (int e = 0; e < 8; e++) v[e] = __fadd_rn(__fmul_rn(d[e], sj), xl[e]);
-            const float so = requant_segment<kOut>(v, blk * 128 + hl * 8, blk < nblk, q, out);
-            collect_scale(so, j, lane, mine);
-        }
-        if (lane_blk_ok) s[b0 + lane] = mine;
-    }
+    const HopOp<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
-int64_t chunks_of(int64_t nblk) { return (nblk + kChunkBlocks - 1) / kChunkBlocks; }
+// Segments per warp chunk for each kernel (tuned on GB300; overridable at build time).
+#ifndef BQ_SEGS_QUANT
+#define BQ_SEGS_QUANT 4
+#endif
+#ifndef BQ_SEGS_DEQUANT
+#define BQ_SEGS_DEQUANT 8
+#endif
+#ifndef BQ_SEGS_ACCUM
+#define BQ_SEGS_ACCUM 4
+#endif
+#ifndef BQ_SEGS_HOP
+#define BQ_SEGS_HOP 4
+#endif
+constexpr int kSegsQuant = BQ_SEGS_QUANT;
+constexpr int kSegsDequant = BQ_SEGS_DEQUANT;
+constexpr int kSegsAccum = BQ_SEGS_ACCUM;
+constexpr int kSegsHop = BQ_SEGS_HOP;
 
-}  // namespace
+int64_t chunks(int64_t nblk, int segs) { return (nblk + 2 * segs - 1) / (2 * segs); }
 
 #define BQK_GRID(kernel, nchunk)                                          \
     int grid = 0;                                                         \
     if (cudaError_t e_ = grid_for((const void *)(kernel), (nchunk), &grid)) \
         return e_;
 
+template <int W, bool kOut>
+cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
+                           cudaStream_t st)
+{
+    auto kernel = accum_i8_kernel<kSegsAccum, W, kOut>;
+    BQK_GRID(kernel, chunks(nblk, kSegsAccum));
+    kernel<<<grid, kThreads, 0, st>>>(src, nsrc, nblk, q, s, out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
 {
-    BQK_GRID(quant_i8_kernel, chunks_of(nblk));
-    quant_i8_kernel<<<grid, kThreads, 0, st>>>(x, nblk, q, s);
+    BQK_GRID(quant_i8_kernel<kSegsQuant>, chunks(nblk, kSegsQuant));
+    quant_i8_kernel<kSegsQuant><<<grid, kThreads, 0, st>>>(x, nblk, q, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
 {
-    BQK_GRID(dequant_i8_kernel, chunks_of(nblk));
-    dequant_i8_kernel<<<grid, kThreads, 0, st>>>(q, s, nblk, out);
+    BQK_GRID(dequant_i8_kernel<kSegsDequant>, chunks(nblk, kSegsDequant));
+    dequant_i8_kernel<kSegsDequant><<<grid, kThreads, 0, st>>>(q, s, nblk, out);
     return cudaGetLastError();
 }
 
+// One source width is compiled per common case (1, 2, 3, 4 sources at once); more
+// sources run in groups of four.
 cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                             cudaStream_t st)
 {
-    if (out) {
-        BQK_GRID(accum_i8_kernel<true>, chunks_of(nblk));
-        accum_i8_kernel<true><<<grid, kThreads, 0, st>>>(src, W, nblk, q, s, out);
-    } else {
-        BQK_GRID(accum_i8_kernel<false>, chunks_of(nblk));
-        accum_i8_kernel<false><<<grid, kThreads, 0, st>>>(src, W, nblk, q, s, nullptr);
+    const bool o = out != nullptr;
+    switch (W) {
+    case 1: return o ? launch_accum_w<1, true>(src, W, nblk, q, s, out, st) : launch_accum_w<1, false>(src, W, nblk, q, s, out, st);
+    case 2: return o ? launch_accum_w<2, true>(src, W, nblk, q, s, out, st) : launch_accum_w<2, false>(src, W, nblk, q, s, out, st);
+    case 3: return o ? launch_accum_w<3, true>(src, W, nblk, q, s, out, st) : launch_accum_w<3, false>(src, W, nblk, q, s, out, st);
+    default: return o ? launch_accum_w<4, true>(src, W, nblk, q, s, out, st) : launch_accum_w<4, false>(src, W, nblk, q, s, out, st);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint16_t *x, int64_t nblk, int8_t *q,
                                float *s, uint16_t *out, cudaStream_t st)
 {
     if (out) {
-        BQK_GRID(ring_hop_i8_kernel<true>, chunks_of(nblk));
-        ring_hop_i8_kernel<true><<<grid, kThreads, 0, st>>>(q_in, s_in, x, nblk, q, s, out);
+        BQK_GRID((ring_hop_i8_kernel<kSegsHop, true>), chunks(nblk, kSegsHop));
+        ring_hop_i8_kernel<kSegsHop, true><<<grid, kThreads, 0, st>>>(q_in, s_in, x, nblk, q, s, out);
     } else {
-        BQK_GRID(ring_hop_i8_kernel<false>, chunks_of(nblk));
-        ring_hop_i8_kernel<false><<<grid, kThreads, 0, st>>>(q_in, s_in, x, nblk, q, s, nullptr);
+        BQK_GRID((ring_hop_i8_kernel<kSegsHop, false>), chunks(nblk, kSegsHop));
+        ring_hop_i8_kernel<kSegsHop, false><<<grid, kThreads, 0, st>>>(q_in, s_in, x, nblk, q, s, nullptr);
     }
     return cudaGetLastError();
 }

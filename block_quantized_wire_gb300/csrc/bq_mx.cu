@@ -19,7 +19,7 @@ namespace {
 __device__ __forceinline__ int64_t first_chunk() { return (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); }
 __device__ __forceinline__ int64_t chunk_stride() { return (int64_t)gridDim.x * (kThreads / 32); }
 
-// Row and 128-column block of linear block index row0 * bpr + cb0 + k.
+// Position (row, 128-column block) of linear block index row0 * bpr + cb0 + k, k >= 0.
 __device__ __forceinline__ void advance(int64_t row0, int64_t cb0, int k, int64_t bpr, int64_t &row, int64_t &cb)
 {
     row = row0;
@@ -30,54 +30,84 @@ __device__ __forceinline__ void advance(int64_t row0, int64_t cb0, int k, int64_
     }
 }
 
+// One warp chunk = 4 segments = 8 blocks = 32 groups of 32 values. After the group
+// amaxes are reduced (4 lanes per group), lane L gathers the amax of the chunk's group
+// L (group order = scale-byte order within the chunk: block-major, 4 groups per
+// block) and computes that group's E8M0 byte and multiplier 2^(127-e) once; each lane
+// then fetches its own group's multiplier per segment, and lanes 4b (b = 0..7) store
+// block b's four scale bytes as one 32-bit word.
+template <bool kTail>
+__device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
+                                               int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
+                                               uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, int64_t row0,
+                                               int64_t cb0, int lane)
+{
+    constexpr int SEGS = kSegs;
+    const int half = lane >> 4, hl = lane & 15;
+    int64_t row[SEGS], cb[SEGS];
+    uint4 raw[SEGS];
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) {
+        advance(row0, cb0, 2 * j + half, bpr, row[j], cb[j]);
+        raw[j] = (!kTail || b0 + 2 * j + half < nblk) ? ld_stream_v4(x + row[j] * ld_x + cb[j] * 128 + hl * 8)
+                                                      : make_uint4(0, 0, 0, 0);
+    }
+    float v[SEGS][8];
+    float gmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) {
+        bf16x8_to_f32(raw[j], v[j]);
+        float m = amax8(v[j]);
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+        const float g = __shfl_sync(kFull, m, (lane & 7) << 2);
+        if ((lane >> 3) == j) gmax = g;
+    }
+    const uint32_t e = mx_scale_byte(gmax);
+    const float p = exp2i(127 - static_cast<int>(e));
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) {
+        const float pj = __shfl_sync(kFull, p, 8 * j + (lane >> 2));
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) y[i] = __fmul_rn(v[j][i], pj);  // exact: a power-of-two scaling
+        if (!kTail || b0 + 2 * j + half < nblk) st_v2(q + row[j] * ld_q + cb[j] * 128 + hl * 8, f32x8_to_e4m3x8(y));
+    }
+    uint32_t word = e << (8 * (lane & 3));
+    word |= __shfl_xor_sync(kFull, word, 1);
+    word |= __shfl_xor_sync(kFull, word, 2);
+    if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk)) {
+        int64_t r, c;
+        advance(row0, cb0, lane >> 2, bpr, r, c);
+        st_u32(s + r * ld_s + c * 4, word);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
                 int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s)
 {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int64_t nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-    for (int64_t c = first_chunk(); c < nchunk; c += chunk_stride()) {
-        const int64_t b0 = c * kChunkBlocks;
-        const int64_t row0 = b0 / bpr, cb0 = b0 - row0 * bpr;
-        uint4 raw[kSegs];
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            int64_t row, cb;
-            advance(row0, cb0, 2 * j + half, bpr, row, cb);
-            raw[j] = (b0 + 2 * j + half < nblk) ? ld_stream_v4(x + row * ld_x + cb * 128 + hl * 8)
-                                                : make_uint4(0, 0, 0, 0);
-        }
-        uint32_t mine = 0;
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            int64_t row, cb;
-            advance(row0, cb0, 2 * j + half, bpr, row, cb);
-            float v[8];
-            bf16x8_to_f32(raw[j], v);
-            float m = amax8(v);
-            m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));  // the 4 lanes of a 32-value group
-            m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
-            const uint32_t e = mx_scale_byte(m);
-            const float p = exp2i(127 - static_cast<int>(e));
-            float y[8];
-#pragma unroll
-            for (int i = 0; i < 8; i++) y[i] = __fmul_rn(v[i], p);  // exact: a power-of-two scaling
-            if (b0 + 2 * j + half < nblk) st_v2(q + row * ld_q + cb * 128 + hl * 8, f32x8_to_e4m3x8(y));
-            // the block's four scale bytes, group g in byte g
-            uint32_t word = e << (8 * (hl >> 2));
-            word |= __shfl_xor_sync(kFull, word, 4);
-            word |= __shfl_xor_sync(kFull, word, 8);
-            const uint32_t lo = __shfl_sync(kFull, word, 0);
-            const uint32_t hi = __shfl_sync(kFull, word, 16);
-            if (lane == 2 * j) mine = lo;
-            if (lane == 2 * j + 1) mine = hi;
-        }
-        if (lane < kChunkBlocks && b0 + lane < nblk) {
-            int64_t row, cb;
-            advance(row0, cb0, lane, bpr, row, cb);
-            st_u32(s + row * ld_s + cb * 4, mine);
+    const int lane = threadIdx.x & 31;
+    const int64_t nfull = nblk / kChunkBlocks;
+    const int64_t stride = ((int64_t)gridDim.x * kThreads) >> 5;
+    int64_t c = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    // block position of this warp's chunk, advanced incrementally by the stride
+    int64_t b0 = c * kChunkBlocks;
+    int64_t row0 = b0 / bpr, cb0 = b0 - row0 * bpr;
+    const int64_t step = stride * kChunkBlocks;
+    const int64_t drow = step / bpr, dcb = step - drow * bpr;
+    for (; c < nfull; c += stride) {
+        quant_mx_chunk<false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, row0, cb0, lane);
+        b0 += step;
+        row0 += drow;
+        cb0 += dcb;
+        if (cb0 >= bpr) {
+            cb0 -= bpr;
+            ++row0;
         }
     }
+    if (c == nfull && nblk % kChunkBlocks)
+        quant_mx_chunk<true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, row0, cb0, lane);
 }
 
 __global__ void __launch_bounds__(kThreads)

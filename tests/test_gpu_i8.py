@@ -275,3 +275,33 @@ def test_errors_surface_before_launch_on_gpu():
     with pytest.raises(BQError) as e:
         codec.quant_i8(x, x.view(torch.int8)[:256], s)  # payload inside x
     assert e.value.status == 4
+
+
+def test_tiny_scale_blocks_across_the_exact_division_cutoff():
+    # Blocks whose amax spans BF16 values from 2^-126 to 2^-90 (scales around 2^-100,
+    # where a kernel's quotient remainders can reach the subnormal range), each with
+    # random values below its amax, including the worst cases found by an exhaustive
+    # sweep of the remainder-based quotient.
+    rng = np.random.default_rng(2024)
+    amax_codes = np.arange(0x0080, 0x12C0, 3, dtype=np.uint16)
+    nblk = amax_codes.size
+    x = np.zeros((nblk, 128), np.uint16)
+    x[:, 0] = amax_codes
+    for b, a in enumerate(amax_codes):
+        x[b, 1:] = rng.integers(0, int(a) + 1, 127).astype(np.uint16) | (rng.integers(0, 2, 127) << 15).astype(np.uint16)
+    x[0, :3] = [0x0438, 0x00EE, 0x00FA]
+    x[1, :3] = [0x0437, 0x00C1, 0x00C5]
+    xb = x.reshape(-1)
+    q, s = gpu_quant(from_bits_bf16(xb))
+    q_ref, s_ref = oracle.quant_i8(xb)
+    assert_same(q, q_ref, "payload")
+    assert_same(s, s_ref, "scales")
+    # the same values as FP32 sums (one source, scale 1 pass-through of tiny values)
+    _, qh, sh = codec.empty_wire_i8(xb.size)
+    zero_q = torch.zeros(xb.size, dtype=torch.int8, device="cuda")
+    zero_s = torch.zeros(xb.size // 128, dtype=torch.float32, device="cuda")
+    codec.ring_hop_i8(zero_q, zero_s, from_bits_bf16(xb), qh, sh, None)
+    qz, sz = oracle.quant_i8(np.zeros_like(xb))
+    qh_r, sh_r, _ = oracle.ring_hop_i8(qz, sz, xb)
+    assert_same(qh, qh_r, "hop payload")
+    assert_same(sh, sh_r, "hop scales")
