@@ -115,53 +115,64 @@ __device__ __forceinline__ void i8x8_to_f32(uint2 w, float (&v)[8])
 }
 
 // ---------------------------------------------------------------- block INT8 scale
-// s = fl(amax / 127) and r = fl(1 / s), both IEEE round-to-nearest, computed once per
-// block. A block with s < 2^-100 (amax below about 1e-28: tiny FP32 sums or tiny BF16
-// inputs) is flagged by r = -1 and quantized with the IEEE division x / s, because
-// there the remainders of i8_quotient could fall into the subnormal range and lose
-// bits; s == 0 gives r = 0, for which the quotient below is 0 and the payload 0.
+// Per block: s = fl(amax / 127) (IEEE division), r = fl(1 / s) (IEEE reciprocal) and
+// rl = fl(fl(1 - s * r) * r), so that r + rl = (1/s)(1 + O(2^-47)). A block with
+// s < 2^-100 (amax below about 1e-28: tiny FP32 sums or tiny BF16 inputs) is flagged
+// by r = -1 and quantized with the IEEE division x / s, because there the remainder
+// of i8_quotient could fall into the subnormal range and lose bits; s == 0 gives
+// r = rl = 0, for which the quotient below is 0 and the payload 0.
 constexpr float kQuotientMinScale = 7.88860905e-31f;  // 2^-100
 
-__device__ __forceinline__ void i8_block_scale(float amax, float &s, float &r)
+struct I8Scale {
+    float s, r, rl;
+};
+
+__device__ __forceinline__ I8Scale i8_block_scale(float amax)
 {
-    s = __fdiv_rn(amax, 127.0f);
-    r = s >= kQuotientMinScale ? __frcp_rn(s) : (s > 0.0f ? -1.0f : 0.0f);
+    I8Scale b;
+    b.s = __fdiv_rn(amax, 127.0f);
+    if (b.s >= kQuotientMinScale) {
+        b.r = __frcp_rn(b.s);
+        b.rl = __fmul_rn(__fmaf_rn(-b.s, b.r, 1.0f), b.r);
+    } else {
+        b.r = b.s > 0.0f ? -1.0f : 0.0f;
+        b.rl = 0.0f;
+    }
+    return b;
 }
 
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
-// fl(x / s) for a normal s with r = fl(1 / s), by Markstein's correction (P. W.
-// Markstein, "Computation of elementary functions on the IBM RISC System/6000
-// processor", IBM J. Res. Develop. 34(1), 1990): when q is within one ulp of x/s and
-// r is the correctly rounded reciprocal, the remainder x - q*s is exact (one FMA) and
-// fl(q + (x - q*s) * r) is the correctly rounded quotient. t0 = fl(x * r) is only
-// known to be within 1.5 ulp, so one correction brings it within an ulp and a second
-// one rounds correctly. |x / s| <= 127.0001 here, so nothing overflows. With s >=
-// 2^-100, a remainder of a quotient >= 1/4 is a multiple of ulp(t) * ulp(s) >= 2^-149
-// and so representable even when subnormal; quotients below 1/4 round to payload 0
-// whatever their last bits.
-__device__ __forceinline__ float i8_quotient(float x, float s, float r)
+// fl(x / s) for s >= 2^-100, by Markstein's correction (P. W. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Develop.
+// 34(1), 1990): when q is within one ulp of x/s and r = fl(1/s), the remainder
+// x - q*s is exact (one FMA) and fl(q + (x - q*s) * r) is the correctly rounded
+// quotient. Here q = fl(x * r + fl(x * rl)) is within 1/2 ulp + 2^-46 relative of x/s
+// because r + rl approximates 1/s to about 2^-47. |x / s| <= 127.0001, so nothing
+// overflows; with s >= 2^-100 the remainder of a quotient >= 1/4 is a multiple of
+// ulp(q) * ulp(s) >= 2^-149 and so representable even when subnormal, and quotients
+// below 1/4 round to payload 0 whatever their last bits.
+__device__ __forceinline__ float i8_quotient(float x, const I8Scale &b)
 {
-    const float t0 = __fmul_rn(x, r);
-    const float t1 = __fmaf_rn(__fmaf_rn(-t0, s, x), r, t0);
-    return __fmaf_rn(__fmaf_rn(-t1, s, x), r, t1);
+    const float q = __fmaf_rn(x, b.r, __fmul_rn(x, b.rl));
+    return __fmaf_rn(__fmaf_rn(-q, b.s, x), b.r, q);
 }
 
-// Quantize eight values of one block with scale s and reciprocal r (i8_block_scale).
-// Returns, per value, the binary32 word M + k (M = 1.5 * 2^23, k the payload integer):
-// adding M to the quotient rounds it to the nearest integer, ties to even, and leaves
-// k in the low mantissa bits, so the word's low byte is k in two's complement and
-// k = word - M exactly. |fl(x/s)| <= fl(amax/s) < 127.5 for a normal s, so no clamp
-// is needed there; the subnormal-s path clamps to [-127, 127].
-__device__ __forceinline__ void i8_quant8(const float (&v)[8], float s, float r, uint32_t (&w)[8])
+// Quantize eight values of one block. Returns, per value, the binary32 word M + k
+// (M = 1.5 * 2^23, k the payload integer): adding M to the quotient rounds it to the
+// nearest integer, ties to even, and leaves k in the low mantissa bits, so the word's
+// low byte is k in two's complement and k = word - M exactly. |fl(x/s)| <=
+// fl(amax/s) < 127.5, so no clamp is needed there; the flagged path clamps to
+// [-127, 127].
+__device__ __forceinline__ void i8_quant8(const float (&v)[8], const I8Scale &b, uint32_t (&w)[8])
 {
-    if (__builtin_expect(r >= 0.0f, 1)) {
+    if (__builtin_expect(b.r >= 0.0f, 1)) {
 #pragma unroll
-        for (int i = 0; i < 8; i++) w[i] = __float_as_uint(__fadd_rn(i8_quotient(v[i], s, r), kMagic));
+        for (int i = 0; i < 8; i++) w[i] = __float_as_uint(__fadd_rn(i8_quotient(v[i], b), kMagic));
     } else {
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            const float k = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -127.0f), 127.0f);
+            const float k = fminf(fmaxf(rintf(__fdiv_rn(v[i], b.s)), -127.0f), 127.0f);
             w[i] = __float_as_uint(__fadd_rn(k, kMagic));
         }
     }

@@ -44,20 +44,21 @@ __device__ __forceinline__ void requant_chunk(const float (&v)[SEGS][8], int64_t
     float m[SEGS];
 #pragma unroll
     for (int j = 0; j < SEGS; j++) m[j] = halfwarp_max(amax8(v[j]));
-    float sc, rc;
-    i8_block_scale(gather_amax<SEGS>(m, lane), sc, rc);
+    const I8Scale mine = i8_block_scale(gather_amax<SEGS>(m, lane));
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
-        const float sj = __shfl_sync(kFull, sc, 2 * j + half);
-        const float rj = __shfl_sync(kFull, rc, 2 * j + half);
+        I8Scale bj;
+        bj.s = __shfl_sync(kFull, mine.s, 2 * j + half);
+        bj.r = __shfl_sync(kFull, mine.r, 2 * j + half);
+        bj.rl = __shfl_sync(kFull, mine.rl, 2 * j + half);
         uint32_t w[8];
-        i8_quant8(v[j], sj, rj, w);
+        i8_quant8(v[j], bj, w);
         if (!kTail || b0 + 2 * j + half < nblk) {
             st_v2(q + e0 + 256 * j, pack_payload8(w));
-            if (kOut) st_v4(out + e0 + 256 * j, i8_materialize_words(w, sj));
+            if (kOut) st_v4(out + e0 + 256 * j, i8_materialize_words(w, bj.s));
         }
     }
-    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) s[b0 + lane] = sc;
+    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) s[b0 + lane] = mine.s;
 }
 
 // Grid-stride driver over warp chunks. With kPrefetch, the loads of a warp's next

@@ -16,9 +16,6 @@
 namespace bqk {
 namespace {
 
-__device__ __forceinline__ int64_t first_chunk() { return (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); }
-__device__ __forceinline__ int64_t chunk_stride() { return (int64_t)gridDim.x * (kThreads / 32); }
-
 // Position (row, 128-column block) of linear block index row0 * bpr + cb0 + k, k >= 0.
 __device__ __forceinline__ void advance(int64_t row0, int64_t cb0, int k, int64_t bpr, int64_t &row, int64_t &cb)
 {
@@ -30,6 +27,25 @@ __device__ __forceinline__ void advance(int64_t row0, int64_t cb0, int k, int64_
     }
 }
 
+// Element offsets of the blocks a lane touches in one chunk of kChunkBlocks blocks that
+// starts at (row0, cb0): off[j] for segment j (block 2j + half), for each of up to three
+// row-major arrays with leading dimensions ld[a] (in elements, or bytes for byte
+// arrays) and per-block widths wid[a] (128 values or 4 scale bytes). A chunk that lies
+// in one row (the common case: 8 of the row's cols/128 blocks) takes one multiply per
+// array; a chunk that crosses rows walks the block positions.
+struct ChunkPos {
+    int64_t row0, cb0;
+};
+
+__device__ __forceinline__ int64_t block_offset(const ChunkPos &p, int k, int64_t bpr, int64_t ld, int64_t wid,
+                                                bool one_row)
+{
+    if (one_row) return p.row0 * ld + (p.cb0 + k) * wid;
+    int64_t r, c;
+    advance(p.row0, p.cb0, k, bpr, r, c);
+    return r * ld + c * wid;
+}
+
 // One warp chunk = 4 segments = 8 blocks = 32 groups of 32 values. After the group
 // amaxes are reduced (4 lanes per group), lane L gathers the amax of the chunk's group
 // L (group order = scale-byte order within the chunk: block-major, 4 groups per
@@ -39,18 +55,17 @@ __device__ __forceinline__ void advance(int64_t row0, int64_t cb0, int k, int64_
 template <bool kTail>
 __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
                                                int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
-                                               uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, int64_t row0,
-                                               int64_t cb0, int lane)
+                                               uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
+                                               int lane)
 {
     constexpr int SEGS = kSegs;
     const int half = lane >> 4, hl = lane & 15;
-    int64_t row[SEGS], cb[SEGS];
+    const bool one_row = pos.cb0 + kChunkBlocks <= bpr;  // warp-uniform
     uint4 raw[SEGS];
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
-        advance(row0, cb0, 2 * j + half, bpr, row[j], cb[j]);
-        raw[j] = (!kTail || b0 + 2 * j + half < nblk) ? ld_stream_v4(x + row[j] * ld_x + cb[j] * 128 + hl * 8)
-                                                      : make_uint4(0, 0, 0, 0);
+        const int64_t ox = block_offset(pos, 2 * j + half, bpr, ld_x, 128, one_row);
+        raw[j] = (!kTail || b0 + 2 * j + half < nblk) ? ld_stream_v4(x + ox + hl * 8) : make_uint4(0, 0, 0, 0);
     }
     float v[SEGS][8];
     float gmax = 0.0f;
@@ -71,17 +86,48 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
         float y[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) y[i] = __fmul_rn(v[j][i], pj);  // exact: a power-of-two scaling
-        if (!kTail || b0 + 2 * j + half < nblk) st_v2(q + row[j] * ld_q + cb[j] * 128 + hl * 8, f32x8_to_e4m3x8(y));
+        if (!kTail || b0 + 2 * j + half < nblk) {
+            const int64_t oq = block_offset(pos, 2 * j + half, bpr, ld_q, 128, one_row);
+            st_v2(q + oq + hl * 8, f32x8_to_e4m3x8(y));
+        }
     }
     uint32_t word = e << (8 * (lane & 3));
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
-    if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk)) {
-        int64_t r, c;
-        advance(row0, cb0, lane >> 2, bpr, r, c);
-        st_u32(s + r * ld_s + c * 4, word);
-    }
+    if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk))
+        st_u32(s + block_offset(pos, lane >> 2, bpr, ld_s, 4, one_row), word);
 }
+
+// Grid-stride walk over chunks with the chunk's (row, column block) advanced
+// incrementally: one division per warp at the start instead of one per chunk.
+struct ChunkWalk {
+    int64_t c, stride, b0, step;
+    ChunkPos pos;
+    int64_t drow, dcb, bpr;
+    __device__ __forceinline__ ChunkWalk(int64_t bpr_)
+    {
+        bpr = bpr_;
+        stride = ((int64_t)gridDim.x * kThreads) >> 5;
+        c = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+        b0 = c * kChunkBlocks;
+        pos.row0 = b0 / bpr;
+        pos.cb0 = b0 - pos.row0 * bpr;
+        step = stride * kChunkBlocks;
+        drow = step / bpr;
+        dcb = step - drow * bpr;
+    }
+    __device__ __forceinline__ void next()
+    {
+        c += stride;
+        b0 += step;
+        pos.row0 += drow;
+        pos.cb0 += dcb;
+        if (pos.cb0 >= bpr) {
+            pos.cb0 -= bpr;
+            ++pos.row0;
+        }
+    }
+};
 
 __global__ void __launch_bounds__(kThreads)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
@@ -89,57 +135,52 @@ quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64
 {
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
-    const int64_t stride = ((int64_t)gridDim.x * kThreads) >> 5;
-    int64_t c = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    // block position of this warp's chunk, advanced incrementally by the stride
-    int64_t b0 = c * kChunkBlocks;
-    int64_t row0 = b0 / bpr, cb0 = b0 - row0 * bpr;
-    const int64_t step = stride * kChunkBlocks;
-    const int64_t drow = step / bpr, dcb = step - drow * bpr;
-    for (; c < nfull; c += stride) {
-        quant_mx_chunk<false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, row0, cb0, lane);
-        b0 += step;
-        row0 += drow;
-        cb0 += dcb;
-        if (cb0 >= bpr) {
-            cb0 -= bpr;
-            ++row0;
+    ChunkWalk w(bpr);
+    for (; w.c < nfull; w.next()) quant_mx_chunk<false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+    if (w.c == nfull && nblk % kChunkBlocks) quant_mx_chunk<true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+}
+
+template <bool kTail>
+__device__ __forceinline__ void dequant_mx_chunk(const uint8_t *__restrict__ q, int64_t ld_q,
+                                                 const uint8_t *__restrict__ s, int64_t ld_s, int64_t bpr,
+                                                 int64_t nblk, uint16_t *__restrict__ out, int64_t ld_out,
+                                                 int64_t b0, ChunkPos pos, int lane)
+{
+    const int half = lane >> 4, hl = lane & 15;
+    const bool one_row = pos.cb0 + kChunkBlocks <= bpr;  // warp-uniform
+    uint2 raw[kSegs];
+    uint32_t sw[kSegs];
+#pragma unroll
+    for (int j = 0; j < kSegs; j++) {
+        const bool ok = !kTail || b0 + 2 * j + half < nblk;
+        const int64_t oq = block_offset(pos, 2 * j + half, bpr, ld_q, 128, one_row);
+        const int64_t os = block_offset(pos, 2 * j + half, bpr, ld_s, 4, one_row);
+        raw[j] = ok ? ld_stream_v2(q + oq + hl * 8) : make_uint2(0, 0);
+        sw[j] = ok ? ld_stream_u32(s + os) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kSegs; j++) {
+        const uint32_t e = (sw[j] >> (8 * (hl >> 2))) & 0xffu;
+        const float p = e == 255u ? __uint_as_float(0x7fc00000u) : exp2i(static_cast<int>(e) - 127);
+        float v[8];
+        e4m3x8_to_f32(raw[j], p, v);
+        if (!kTail || b0 + 2 * j + half < nblk) {
+            const int64_t oo = block_offset(pos, 2 * j + half, bpr, ld_out, 128, one_row);
+            st_v4(out + oo + hl * 8, f32x8_to_bf16x8(v));
         }
     }
-    if (c == nfull && nblk % kChunkBlocks)
-        quant_mx_chunk<true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, row0, cb0, lane);
 }
 
 __global__ void __launch_bounds__(kThreads)
 dequant_mx_kernel(const uint8_t *__restrict__ q, int64_t ld_q, const uint8_t *__restrict__ s, int64_t ld_s,
                   int64_t bpr, int64_t nblk, uint16_t *__restrict__ out, int64_t ld_out)
 {
-    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
-    const int64_t nchunk = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-    for (int64_t c = first_chunk(); c < nchunk; c += chunk_stride()) {
-        const int64_t b0 = c * kChunkBlocks;
-        const int64_t row0 = b0 / bpr, cb0 = b0 - row0 * bpr;
-        uint2 raw[kSegs];
-        uint32_t sw[kSegs];
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            int64_t row, cb;
-            advance(row0, cb0, 2 * j + half, bpr, row, cb);
-            const bool ok = b0 + 2 * j + half < nblk;
-            raw[j] = ok ? ld_stream_v2(q + row * ld_q + cb * 128 + hl * 8) : make_uint2(0, 0);
-            sw[j] = ok ? ld_stream_u32(s + row * ld_s + cb * 4) : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < kSegs; j++) {
-            int64_t row, cb;
-            advance(row0, cb0, 2 * j + half, bpr, row, cb);
-            const uint32_t e = (sw[j] >> (8 * (hl >> 2))) & 0xffu;
-            const float p = e == 255u ? __uint_as_float(0x7fc00000u) : exp2i(static_cast<int>(e) - 127);
-            float v[8];
-            e4m3x8_to_f32(raw[j], p, v);
-            if (b0 + 2 * j + half < nblk) st_v4(out + row * ld_out + cb * 128 + hl * 8, f32x8_to_bf16x8(v));
-        }
-    }
+    const int lane = threadIdx.x & 31;
+    const int64_t nfull = nblk / kChunkBlocks;
+    ChunkWalk w(bpr);
+    for (; w.c < nfull; w.next()) dequant_mx_chunk<false>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
+    if (w.c == nfull && nblk % kChunkBlocks)
+        dequant_mx_chunk<true>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
 }
 
 #define BQK_GRID(kernel, nchunk)                                          \
