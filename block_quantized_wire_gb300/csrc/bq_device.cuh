@@ -64,29 +64,85 @@ __device__ __forceinline__ void st_u32(void *p, uint32_t v)
     asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- packed binary32 pairs
+// A lane's eight values are held as four float2 pairs (values 2i, 2i+1) so that the
+// FP32 arithmetic runs on the paired IEEE instructions of sm_100-class GPUs: each of
+// add2/mul2/fma2 is two independent binary32 operations rounded to nearest even (no
+// flush to zero), bit-identical to two scalar __fadd_rn/__fmul_rn/__fmaf_rn, at one
+// issue slot. They are written as PTX with an explicit .rn so that no multiply is ever
+// fused with a following add: the codec's definitions round every product and every
+// sum separately.
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
+
+// Products that feed a sum (accumulate, ring hop) must round on their own, but the
+// compiler was observed to fuse a paired multiply with a following paired add into one
+// fused multiply-add, explicit .rn and --fmad=false notwithstanding (the fused result
+// showed up in about 13% of random operands). A paired FMA with a +0 addend rounds the
+// product exactly as a multiply does, and it cannot be rewritten into a multiply (it
+// turns a -0 product into +0), so nothing can fuse it with the add that follows. The
+// sign of a zero product never reaches an output here: it only feeds amax and the
+// rounding of a value whose payload is 0.
+__device__ __forceinline__ float2 mul2_unfused(float2 a, float2 b) { return fma2(a, b, splat(0.0f)); }
+
 // ---------------------------------------------------------------- number formats
 // Eight BF16 values (one 16-byte word) widened exactly to binary32.
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float (&v)[8])
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float2 (&v)[4])
 {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        v[2 * i] = __uint_as_float(u[i] << 16);
-        v[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 4; i++) v[i] = make_float2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xffff0000u));
 }
 
-// Two binary32 values rounded to nearest-even BF16, packed (lo in bits 0..15).
-__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
+// Two binary32 values rounded to nearest-even BF16, packed (x in bits 0..15).
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float2 v)
 {
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    __nv_bfloat162 h = __float22bfloat162_rn(v);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ uint4 f32x8_to_bf16x8(const float (&v)[8])
+__device__ __forceinline__ uint4 f32x8_to_bf16x8(const float2 (&v)[4])
 {
-    return make_uint4(f32x2_to_bf16x2(v[0], v[1]), f32x2_to_bf16x2(v[2], v[3]),
-                      f32x2_to_bf16x2(v[4], v[5]), f32x2_to_bf16x2(v[6], v[7]));
+    return make_uint4(f32x2_to_bf16x2(v[0]), f32x2_to_bf16x2(v[1]), f32x2_to_bf16x2(v[2]), f32x2_to_bf16x2(v[3]));
 }
 
 // Low bytes of four 32-bit words, packed little-endian into one word.
@@ -98,20 +154,20 @@ __device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint3
 // Four signed payload bytes (one word) -> their exact binary32 values. Each byte,
 // offset by 128, is placed in the low mantissa bits of 2^23 and the offset removed:
 // (2^23 + q + 128) - (2^23 + 128) = q exactly; q = 0 gives +0.
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *v)
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float2 &lo, float2 &hi)
 {
-    constexpr float kBias = 8388736.0f;  // 2^23 + 128
+    const float2 nbias = splat(-8388736.0f);  // -(2^23 + 128)
     const uint32_t u = w ^ 0x80808080u;
-    v[0] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7540)), kBias);
-    v[1] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7541)), kBias);
-    v[2] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7542)), kBias);
-    v[3] = __fsub_rn(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7543)), kBias);
+    lo = add2(make_float2(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7540)),
+                          __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7541))), nbias);
+    hi = add2(make_float2(__uint_as_float(__byte_perm(u, 0x4b000000u, 0x7542)),
+                          __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7543))), nbias);
 }
 
-__device__ __forceinline__ void i8x8_to_f32(uint2 w, float (&v)[8])
+__device__ __forceinline__ void i8x8_to_f32(uint2 w, float2 (&v)[4])
 {
-    i8x4_to_f32(w.x, v);
-    i8x4_to_f32(w.y, v + 4);
+    i8x4_to_f32(w.x, v[0], v[1]);
+    i8x4_to_f32(w.y, v[2], v[3]);
 }
 
 // ---------------------------------------------------------------- block INT8 scale
@@ -143,19 +199,19 @@ __device__ __forceinline__ I8Scale i8_block_scale(float amax)
 
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
-// fl(x / s) for s >= 2^-100, by Markstein's correction (P. W. Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Develop.
-// 34(1), 1990): when q is within one ulp of x/s and r = fl(1/s), the remainder
-// x - q*s is exact (one FMA) and fl(q + (x - q*s) * r) is the correctly rounded
-// quotient. Here q = fl(x * r + fl(x * rl)) is within 1/2 ulp + 2^-46 relative of x/s
-// because r + rl approximates 1/s to about 2^-47. |x / s| <= 127.0001, so nothing
-// overflows; with s >= 2^-100 the remainder of a quotient >= 1/4 is a multiple of
-// ulp(q) * ulp(s) >= 2^-149 and so representable even when subnormal, and quotients
-// below 1/4 round to payload 0 whatever their last bits.
-__device__ __forceinline__ float i8_quotient(float x, const I8Scale &b)
+// fl(x / s) for s >= 2^-100, two values at a time, by Markstein's correction (P. W.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990): when q is within one ulp of x/s and
+// r = fl(1/s), the remainder x - q*s is exact (one FMA) and fl(q + (x - q*s) * r) is
+// the correctly rounded quotient. Here q = fl(x * r + fl(x * rl)) is within 1/2 ulp +
+// 2^-46 relative of x/s because r + rl approximates 1/s to about 2^-47. |x / s| <=
+// 127.0001, so nothing overflows; with s >= 2^-100 the remainder of a quotient >= 1/4
+// is a multiple of ulp(q) * ulp(s) >= 2^-149 and so representable even when
+// subnormal, and quotients below 1/4 round to payload 0 whatever their last bits.
+__device__ __forceinline__ float2 i8_quotient2(float2 x, float2 r, float2 rl, float2 neg_s)
 {
-    const float q = __fmaf_rn(x, b.r, __fmul_rn(x, b.rl));
-    return __fmaf_rn(__fmaf_rn(-q, b.s, x), b.r, q);
+    const float2 q = fma2(x, r, mul2(x, rl));
+    return fma2(fma2(q, neg_s, x), r, q);
 }
 
 // Quantize eight values of one block. Returns, per value, the binary32 word M + k
@@ -164,15 +220,21 @@ __device__ __forceinline__ float i8_quotient(float x, const I8Scale &b)
 // low byte is k in two's complement and k = word - M exactly. |fl(x/s)| <=
 // fl(amax/s) < 127.5, so no clamp is needed there; the flagged path clamps to
 // [-127, 127].
-__device__ __forceinline__ void i8_quant8(const float (&v)[8], const I8Scale &b, uint32_t (&w)[8])
+__device__ __forceinline__ void i8_quant8(const float2 (&v)[4], const I8Scale &b, uint32_t (&w)[8])
 {
     if (__builtin_expect(b.r >= 0.0f, 1)) {
+        const float2 r = splat(b.r), rl = splat(b.rl), ns = splat(-b.s), m = splat(kMagic);
 #pragma unroll
-        for (int i = 0; i < 8; i++) w[i] = __float_as_uint(__fadd_rn(i8_quotient(v[i], b), kMagic));
+        for (int i = 0; i < 4; i++) {
+            const float2 y = add2(i8_quotient2(v[i], r, rl, ns), m);
+            w[2 * i] = __float_as_uint(y.x);
+            w[2 * i + 1] = __float_as_uint(y.y);
+        }
     } else {
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-            const float k = fminf(fmaxf(rintf(__fdiv_rn(v[i], b.s)), -127.0f), 127.0f);
+            const float x = (i & 1) ? v[i >> 1].y : v[i >> 1].x;
+            const float k = fminf(fmaxf(rintf(__fdiv_rn(x, b.s)), -127.0f), 127.0f);
             w[i] = __float_as_uint(__fadd_rn(k, kMagic));
         }
     }
@@ -183,11 +245,11 @@ __device__ __forceinline__ uint2 pack_payload8(const uint32_t (&w)[8])
     return make_uint2(pack_low_bytes(w[0], w[1], w[2], w[3]), pack_low_bytes(w[4], w[5], w[6], w[7]));
 }
 
-__device__ __forceinline__ float amax8(const float (&v)[8])
+__device__ __forceinline__ float amax8(const float2 (&v)[4])
 {
-    float m = fabsf(v[0]);
+    float m = fmaxf(fabsf(v[0].x), fabsf(v[0].y));
 #pragma unroll
-    for (int i = 1; i < 8; i++) m = fmaxf(m, fabsf(v[i]));
+    for (int i = 1; i < 4; i++) m = fmaxf(m, fmaxf(fabsf(v[i].x), fabsf(v[i].y)));
     return m;
 }
 
@@ -204,18 +266,21 @@ __device__ __forceinline__ float halfwarp_max(float m)
 // BF16 of fl(k * s) for the eight payload integers held as words M + k.
 __device__ __forceinline__ uint4 i8_materialize_words(const uint32_t (&w)[8], float s)
 {
-    float d[8];
+    const float2 nm = splat(-kMagic), s2 = splat(s);
+    float2 d[4];
 #pragma unroll
-    for (int i = 0; i < 8; i++) d[i] = __fmul_rn(__fsub_rn(__uint_as_float(w[i]), kMagic), s);
+    for (int i = 0; i < 4; i++)
+        d[i] = mul2(add2(make_float2(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1])), nm), s2);
     return f32x8_to_bf16x8(d);
 }
 
 // BF16 of fl(q * s) for eight payload integers held as binary32.
-__device__ __forceinline__ uint4 i8_materialize8(const float (&qf)[8], float s)
+__device__ __forceinline__ uint4 i8_materialize8(const float2 (&qf)[4], float s)
 {
-    float d[8];
+    const float2 s2 = splat(s);
+    float2 d[4];
 #pragma unroll
-    for (int i = 0; i < 8; i++) d[i] = __fmul_rn(qf[i], s);
+    for (int i = 0; i < 4; i++) d[i] = mul2(qf[i], s2);
     return f32x8_to_bf16x8(d);
 }
 
@@ -243,18 +308,18 @@ __device__ __forceinline__ float exp2i(int k)
 
 // Eight binary32 values -> eight E4M3 codes (nearest even, saturating), value i in
 // byte i.
-__device__ __forceinline__ uint2 f32x8_to_e4m3x8(const float (&y)[8])
+__device__ __forceinline__ uint2 f32x8_to_e4m3x8(const float2 (&y)[4])
 {
     uint32_t h[4];
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-        h[i] = __nv_cvt_float2_to_fp8x2(make_float2(y[2 * i], y[2 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+    for (int i = 0; i < 4; i++) h[i] = __nv_cvt_float2_to_fp8x2(y[i], __NV_SATFINITE, __NV_E4M3);
     return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
-// Eight E4M3 codes -> their exact binary32 values, each times 2^k (exact).
-__device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float p, float (&v)[8])
+// Eight E4M3 codes -> their exact binary32 values, each times p = 2^k (exact).
+__device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float p, float2 (&v)[4])
 {
+    const float2 p2 = splat(p);
     const uint32_t u[2] = {w.x, w.y};
 #pragma unroll
     for (int j = 0; j < 2; j++) {
@@ -263,9 +328,7 @@ __device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float p, float (&v)[8])
             const __nv_fp8x2_storage_t c = static_cast<__nv_fp8x2_storage_t>((u[j] >> (16 * i)) & 0xffffu);
             const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
             const __half2 hh = *reinterpret_cast<const __half2 *>(&hr);
-            const float2 f = __half22float2(hh);
-            v[4 * j + 2 * i] = __fmul_rn(f.x, p);
-            v[4 * j + 2 * i + 1] = __fmul_rn(f.y, p);
+            v[2 * j + i] = mul2(__half22float2(hh), p2);
         }
     }
 }

@@ -36,7 +36,7 @@ __device__ __forceinline__ float gather_amax(const float (&m)[SEGS], int lane)
 // Requantize SEGS segments of FP32 values (v[j] = lane's 8 values of segment j):
 // writes the payload, the chunk's scales and, when kOut, the BF16 materialization.
 template <int SEGS, bool kTail, bool kOut>
-__device__ __forceinline__ void requant_chunk(const float (&v)[SEGS][8], int64_t e0, int64_t b0, int64_t nblk,
+__device__ __forceinline__ void requant_chunk(const float2 (&v)[SEGS][4], int64_t e0, int64_t b0, int64_t nblk,
                                               int lane, int8_t *__restrict__ q, float *__restrict__ s,
                                               uint16_t *__restrict__ out)
 {
@@ -124,7 +124,7 @@ struct QuantOp {
     template <bool kTail>
     __device__ __forceinline__ void compute(const In &in, int64_t c) const
     {
-        float v[SEGS][8];
+        float2 v[SEGS][4];
 #pragma unroll
         for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
         requant_chunk<SEGS, kTail, false>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, nullptr);
@@ -169,7 +169,7 @@ struct DequantOp {
 #pragma unroll
         for (int j = 0; j < SEGS; j++) {
             const float sj = __shfl_sync(kFull, in.sc, 2 * j + half);
-            float v[8];
+            float2 v[4];
             i8x8_to_f32(in.q[j], v);
             if (!kTail || b0 + 2 * j + half < nblk) st_v4(out + e0 + 256 * j, i8_materialize8(v, sj));
         }
@@ -214,7 +214,7 @@ __device__ __forceinline__ void load_sources(SourceRegs<SEGS, W> &r, const Sourc
 }
 
 template <int SEGS, int W, bool kFirst>
-__device__ __forceinline__ void add_sources(const SourceRegs<SEGS, W> &r, int g, int nsrc, float (&acc)[SEGS][8],
+__device__ __forceinline__ void add_sources(const SourceRegs<SEGS, W> &r, int g, int nsrc, float2 (&acc)[SEGS][4],
                                             int lane)
 {
     const int half = lane >> 4;
@@ -223,13 +223,13 @@ __device__ __forceinline__ void add_sources(const SourceRegs<SEGS, W> &r, int g,
         if (g + i >= nsrc) break;
 #pragma unroll
         for (int j = 0; j < SEGS; j++) {
-            const float sj = __shfl_sync(kFull, r.sc[i], 2 * j + half);
-            float v[8];
+            const float2 sj = splat(__shfl_sync(kFull, r.sc[i], 2 * j + half));
+            float2 v[4];
             i8x8_to_f32(r.q[i][j], v);
 #pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const float d = __fmul_rn(v[e], sj);
-                acc[j][e] = (kFirst && i == 0) ? d : __fadd_rn(acc[j][e], d);
+            for (int e = 0; e < 4; e++) {
+                const float2 d = mul2_unfused(v[e], sj);
+                acc[j][e] = (kFirst && i == 0) ? d : add2(acc[j][e], d);
             }
         }
     }
@@ -253,7 +253,7 @@ struct AccumOp {
     template <bool kTail>
     __device__ __forceinline__ void compute(const In &in, int64_t c) const
     {
-        float acc[SEGS][8];
+        float2 acc[SEGS][4];
         add_sources<SEGS, W, true>(in, 0, nsrc, acc, lane);
         for (int g = W; g < nsrc; g += W) {
             In more;
@@ -306,15 +306,15 @@ struct HopOp {
     __device__ __forceinline__ void compute(const In &in, int64_t c) const
     {
         const int half = lane >> 4;
-        float v[SEGS][8];
+        float2 v[SEGS][4];
 #pragma unroll
         for (int j = 0; j < SEGS; j++) {
-            const float sj = __shfl_sync(kFull, in.sc, 2 * j + half);
-            float d[8], xl[8];
+            const float2 sj = splat(__shfl_sync(kFull, in.sc, 2 * j + half));
+            float2 d[4], xl[4];
             i8x8_to_f32(in.q[j], d);
             bf16x8_to_f32(in.x[j], xl);
 #pragma unroll
-            for (int e = 0; e < 8; e++) v[j][e] = __fadd_rn(__fmul_rn(d[e], sj), xl[e]);
+            for (int e = 0; e < 4; e++) v[j][e] = add2(mul2_unfused(d[e], sj), xl[e]);
         }
         requant_chunk<SEGS, kTail, kOut>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, out);
     }

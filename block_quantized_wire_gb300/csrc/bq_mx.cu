@@ -67,7 +67,7 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
         const int64_t ox = block_offset(pos, 2 * j + half, bpr, ld_x, 128, one_row);
         raw[j] = (!kTail || b0 + 2 * j + half < nblk) ? ld_stream_v4(x + ox + hl * 8) : make_uint4(0, 0, 0, 0);
     }
-    float v[SEGS][8];
+    float2 v[SEGS][4];
     float gmax = 0.0f;
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
@@ -82,10 +82,10 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
     const float p = exp2i(127 - static_cast<int>(e));
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
-        const float pj = __shfl_sync(kFull, p, 8 * j + (lane >> 2));
-        float y[8];
+        const float2 pj = splat(__shfl_sync(kFull, p, 8 * j + (lane >> 2)));
+        float2 y[4];
 #pragma unroll
-        for (int i = 0; i < 8; i++) y[i] = __fmul_rn(v[j][i], pj);  // exact: a power-of-two scaling
+        for (int i = 0; i < 4; i++) y[i] = mul2(v[j][i], pj);  // exact: a power-of-two scaling
         if (!kTail || b0 + 2 * j + half < nblk) {
             const int64_t oq = block_offset(pos, 2 * j + half, bpr, ld_q, 128, one_row);
             st_v2(q + oq + hl * 8, f32x8_to_e4m3x8(y));
@@ -162,7 +162,7 @@ __device__ __forceinline__ void dequant_mx_chunk(const uint8_t *__restrict__ q, 
     for (int j = 0; j < kSegs; j++) {
         const uint32_t e = (sw[j] >> (8 * (hl >> 2))) & 0xffu;
         const float p = e == 255u ? __uint_as_float(0x7fc00000u) : exp2i(static_cast<int>(e) - 127);
-        float v[8];
+        float2 v[4];
         e4m3x8_to_f32(raw[j], p, v);
         if (!kTail || b0 + 2 * j + half < nblk) {
             const int64_t oo = block_offset(pos, 2 * j + half, bpr, ld_out, 128, one_row);
