@@ -22,6 +22,15 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSegs = 4;                      // segments per warp iteration
 constexpr int kChunkBlocks = 2 * kSegs;       // 128-value blocks per warp iteration
 
+// ---------------------------------------------------------------- launch ordering
+// First statement of every codec kernel (see launch_kernel in bq_launch.h): wait for
+// the previous grid's completion and memory, then let the next grid start launching.
+__device__ __forceinline__ void pdl_begin()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- global memory
 // Inputs are read once: non-coherent path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)

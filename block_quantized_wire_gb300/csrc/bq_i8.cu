@@ -135,6 +135,7 @@ template <int SEGS>
 __global__ void __launch_bounds__(kThreads)
 quant_i8_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
+    pdl_begin();
     const QuantOp<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -180,6 +181,7 @@ template <int SEGS>
 __global__ void __launch_bounds__(kThreads)
 dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk, uint16_t *__restrict__ out)
 {
+    pdl_begin();
     const DequantOp<SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<true>(op, nblk, 2 * SEGS);
 }
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(kThreads)
 accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s,
                 uint16_t *__restrict__ out)
 {
+    pdl_begin();
     const AccumOp<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(kThreads)
 ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_in, const uint16_t *__restrict__ x,
                    int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s, uint16_t *__restrict__ out)
 {
+    pdl_begin();
     const HopOp<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -360,8 +364,7 @@ cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t
 {
     auto kernel = accum_i8_kernel<kSegsAccum, W, kOut>;
     BQK_GRID(kernel, chunks(nblk, kSegsAccum));
-    kernel<<<grid, kThreads, 0, st>>>(src, nsrc, nblk, q, s, out);
-    return cudaGetLastError();
+    return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
 }
 
 }  // namespace
@@ -369,15 +372,13 @@ cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t
 cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
 {
     BQK_GRID(quant_i8_kernel<kSegsQuant>, chunks(nblk, kSegsQuant));
-    quant_i8_kernel<kSegsQuant><<<grid, kThreads, 0, st>>>(x, nblk, q, s);
-    return cudaGetLastError();
+    return launch_kernel(quant_i8_kernel<kSegsQuant>, grid, st, x, nblk, q, s);
 }
 
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
 {
     BQK_GRID(dequant_i8_kernel<kSegsDequant>, chunks(nblk, kSegsDequant));
-    dequant_i8_kernel<kSegsDequant><<<grid, kThreads, 0, st>>>(q, s, nblk, out);
-    return cudaGetLastError();
+    return launch_kernel(dequant_i8_kernel<kSegsDequant>, grid, st, q, s, nblk, out);
 }
 
 // One source width is compiled per common case (1, 2, 3, 4 sources at once); more
@@ -399,12 +400,11 @@ cudaError_t launch_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint
 {
     if (out) {
         BQK_GRID((ring_hop_i8_kernel<kSegsHop, true>), chunks(nblk, kSegsHop));
-        ring_hop_i8_kernel<kSegsHop, true><<<grid, kThreads, 0, st>>>(q_in, s_in, x, nblk, q, s, out);
-    } else {
-        BQK_GRID((ring_hop_i8_kernel<kSegsHop, false>), chunks(nblk, kSegsHop));
-        ring_hop_i8_kernel<kSegsHop, false><<<grid, kThreads, 0, st>>>(q_in, s_in, x, nblk, q, s, nullptr);
+        return launch_kernel(ring_hop_i8_kernel<kSegsHop, true>, grid, st, q_in, s_in, x, nblk, q, s, out);
     }
-    return cudaGetLastError();
+    BQK_GRID((ring_hop_i8_kernel<kSegsHop, false>), chunks(nblk, kSegsHop));
+    return launch_kernel(ring_hop_i8_kernel<kSegsHop, false>, grid, st, q_in, s_in, x, nblk, q, s,
+                         static_cast<uint16_t *>(nullptr));
 }
 
 }  // namespace bqk

@@ -29,6 +29,33 @@ cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, 
                               int64_t rows, int64_t cols, uint16_t *out, int64_t ld_out,
                               cudaStream_t st);
 
+// Programmatic dependent launch: every codec kernel is launched with programmatic
+// stream serialization and begins with griddepcontrol.wait, which returns once the
+// previous grid in the stream has completed and its memory is visible. The kernel then
+// allows its own dependents to launch, so the next codec call's launch and CTA
+// placement overlap this kernel's tail instead of following it. Ordering against any
+// other work is unchanged: a kernel that does not trigger (not one of these) is
+// waited for in full.
+#ifndef BQ_PDL
+#define BQ_PDL 1
+#endif
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = BQ_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Grid size for a grid-stride kernel over `nchunk` warp chunks: enough CTAs to fill
 // every SM of the current device at the kernel's occupancy, and no more CTAs than
 // there are chunks. Returns the error of the device queries, if any.

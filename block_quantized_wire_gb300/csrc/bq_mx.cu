@@ -37,10 +37,13 @@ struct ChunkPos {
     int64_t row0, cb0;
 };
 
-__device__ __forceinline__ int64_t block_offset(const ChunkPos &p, int k, int64_t bpr, int64_t ld, int64_t wid,
-                                                bool one_row)
+// Offset of block k of the chunk in a row-major array with leading dimension ld and
+// per-block width wid. kOneRow (the chunk lies in one row, decided per chunk and
+// warp-uniform) makes it base + k * wid with the base shared by all blocks.
+template <bool kOneRow>
+__device__ __forceinline__ int64_t block_offset(const ChunkPos &p, int k, int64_t bpr, int64_t ld, int64_t wid)
 {
-    if (one_row) return p.row0 * ld + (p.cb0 + k) * wid;
+    if (kOneRow) return p.row0 * ld + p.cb0 * wid + k * wid;
     int64_t r, c;
     advance(p.row0, p.cb0, k, bpr, r, c);
     return r * ld + c * wid;
@@ -52,7 +55,7 @@ __device__ __forceinline__ int64_t block_offset(const ChunkPos &p, int k, int64_
 // block) and computes that group's E8M0 byte and multiplier 2^(127-e) once; each lane
 // then fetches its own group's multiplier per segment, and lanes 4b (b = 0..7) store
 // block b's four scale bytes as one 32-bit word.
-template <bool kTail>
+template <bool kTail, bool kOneRow>
 __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
                                                int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
                                                uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
@@ -60,11 +63,10 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
 {
     constexpr int SEGS = kSegs;
     const int half = lane >> 4, hl = lane & 15;
-    const bool one_row = pos.cb0 + kChunkBlocks <= bpr;  // warp-uniform
     uint4 raw[SEGS];
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
-        const int64_t ox = block_offset(pos, 2 * j + half, bpr, ld_x, 128, one_row);
+        const int64_t ox = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_x, 128);
         raw[j] = (!kTail || b0 + 2 * j + half < nblk) ? ld_stream_v4(x + ox + hl * 8) : make_uint4(0, 0, 0, 0);
     }
     float2 v[SEGS][4];
@@ -87,7 +89,7 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
 #pragma unroll
         for (int i = 0; i < 4; i++) y[i] = mul2(v[j][i], pj);  // exact: a power-of-two scaling
         if (!kTail || b0 + 2 * j + half < nblk) {
-            const int64_t oq = block_offset(pos, 2 * j + half, bpr, ld_q, 128, one_row);
+            const int64_t oq = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_q, 128);
             st_v2(q + oq + hl * 8, f32x8_to_e4m3x8(y));
         }
     }
@@ -95,7 +97,19 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
     if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk))
-        st_u32(s + block_offset(pos, lane >> 2, bpr, ld_s, 4, one_row), word);
+        st_u32(s + block_offset<kOneRow>(pos, lane >> 2, bpr, ld_s, 4), word);
+}
+
+template <bool kTail>
+__device__ __forceinline__ void quant_mx_chunk_any(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
+                                                   int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
+                                                   uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
+                                                   int lane)
+{
+    if (pos.cb0 + kChunkBlocks <= bpr)
+        quant_mx_chunk<kTail, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
+    else
+        quant_mx_chunk<kTail, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
 }
 
 // Grid-stride walk over chunks with the chunk's (row, column block) advanced
@@ -133,28 +147,29 @@ __global__ void __launch_bounds__(kThreads)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
                 int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s)
 {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
     ChunkWalk w(bpr);
-    for (; w.c < nfull; w.next()) quant_mx_chunk<false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
-    if (w.c == nfull && nblk % kChunkBlocks) quant_mx_chunk<true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+    for (; w.c < nfull; w.next()) quant_mx_chunk_any<false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+    if (w.c == nfull && nblk % kChunkBlocks)
+        quant_mx_chunk_any<true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
 }
 
-template <bool kTail>
+template <bool kTail, bool kOneRow>
 __device__ __forceinline__ void dequant_mx_chunk(const uint8_t *__restrict__ q, int64_t ld_q,
                                                  const uint8_t *__restrict__ s, int64_t ld_s, int64_t bpr,
                                                  int64_t nblk, uint16_t *__restrict__ out, int64_t ld_out,
                                                  int64_t b0, ChunkPos pos, int lane)
 {
     const int half = lane >> 4, hl = lane & 15;
-    const bool one_row = pos.cb0 + kChunkBlocks <= bpr;  // warp-uniform
     uint2 raw[kSegs];
     uint32_t sw[kSegs];
 #pragma unroll
     for (int j = 0; j < kSegs; j++) {
         const bool ok = !kTail || b0 + 2 * j + half < nblk;
-        const int64_t oq = block_offset(pos, 2 * j + half, bpr, ld_q, 128, one_row);
-        const int64_t os = block_offset(pos, 2 * j + half, bpr, ld_s, 4, one_row);
+        const int64_t oq = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_q, 128);
+        const int64_t os = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_s, 4);
         raw[j] = ok ? ld_stream_v2(q + oq + hl * 8) : make_uint2(0, 0);
         sw[j] = ok ? ld_stream_u32(s + os) : 0u;
     }
@@ -165,22 +180,36 @@ __device__ __forceinline__ void dequant_mx_chunk(const uint8_t *__restrict__ q, 
         float2 v[4];
         e4m3x8_to_f32(raw[j], p, v);
         if (!kTail || b0 + 2 * j + half < nblk) {
-            const int64_t oo = block_offset(pos, 2 * j + half, bpr, ld_out, 128, one_row);
+            const int64_t oo = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_out, 128);
             st_v4(out + oo + hl * 8, f32x8_to_bf16x8(v));
         }
     }
+}
+
+template <bool kTail>
+__device__ __forceinline__ void dequant_mx_chunk_any(const uint8_t *__restrict__ q, int64_t ld_q,
+                                                     const uint8_t *__restrict__ s, int64_t ld_s, int64_t bpr,
+                                                     int64_t nblk, uint16_t *__restrict__ out, int64_t ld_out,
+                                                     int64_t b0, ChunkPos pos, int lane)
+{
+    if (pos.cb0 + kChunkBlocks <= bpr)
+        dequant_mx_chunk<kTail, true>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, b0, pos, lane);
+    else
+        dequant_mx_chunk<kTail, false>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, b0, pos, lane);
 }
 
 __global__ void __launch_bounds__(kThreads)
 dequant_mx_kernel(const uint8_t *__restrict__ q, int64_t ld_q, const uint8_t *__restrict__ s, int64_t ld_s,
                   int64_t bpr, int64_t nblk, uint16_t *__restrict__ out, int64_t ld_out)
 {
+    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
     ChunkWalk w(bpr);
-    for (; w.c < nfull; w.next()) dequant_mx_chunk<false>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
+    for (; w.c < nfull; w.next())
+        dequant_mx_chunk_any<false>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
     if (w.c == nfull && nblk % kChunkBlocks)
-        dequant_mx_chunk<true>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
+        dequant_mx_chunk_any<true>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
 }
 
 #define BQK_GRID(kernel, nchunk)                                          \
@@ -195,8 +224,7 @@ cudaError_t launch_quant_mx(const uint16_t *x, int64_t ld_x, int64_t rows, int64
 {
     const int64_t bpr = cols / 128, nblk = rows * bpr;
     BQK_GRID(quant_mx_kernel, (nblk + kChunkBlocks - 1) / kChunkBlocks);
-    quant_mx_kernel<<<grid, kThreads, 0, st>>>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
-    return cudaGetLastError();
+    return launch_kernel(quant_mx_kernel, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
 }
 
 cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_s, int64_t rows,
@@ -204,8 +232,7 @@ cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, 
 {
     const int64_t bpr = cols / 128, nblk = rows * bpr;
     BQK_GRID(dequant_mx_kernel, (nblk + kChunkBlocks - 1) / kChunkBlocks);
-    dequant_mx_kernel<<<grid, kThreads, 0, st>>>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out);
-    return cudaGetLastError();
+    return launch_kernel(dequant_mx_kernel, grid, st, q, ld_q, s, ld_s, bpr, nblk, out, ld_out);
 }
 
 }  // namespace bqk
