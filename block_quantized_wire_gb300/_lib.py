@@ -31,6 +31,8 @@ _PROTOS = {
     "bq_ring_hop_i8": ([_P, _P, _P, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_quant_mx": ([_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
     "bq_dequant_mx": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "bq_take_wait_timeouts": ([_P], ctypes.c_int),
+    "bq_selftest_wait_timeout": ([_P], ctypes.c_int),
 }
 
 

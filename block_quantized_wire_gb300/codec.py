@@ -155,3 +155,17 @@ def dequant_mx(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor, stream=None)
     if (sr, sc) != (rows, cols // GROUP_MX) or (orr, oc) != (rows, cols):
         raise ValueError("dequant_mx: shapes do not match")
     check("bq_dequant_mx", load().bq_dequant_mx(qp, ld_q, sp, ld_s, rows, cols, op, ld_o, _stream(stream)))
+
+
+# ---------------------------------------------------------------- bounded waits
+def take_wait_timeouts() -> int:
+    """Waits inside codec kernels that ran out (1 s limit) since the last call; resets the
+    count. Synchronizes with the device."""
+    n = ctypes.c_int64(0)
+    check("bq_take_wait_timeouts", load().bq_take_wait_timeouts(ctypes.byref(n)))
+    return int(n.value)
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Run one deliberately unsatisfied 20 ms bounded wait (the count grows by one)."""
+    check("bq_selftest_wait_timeout", load().bq_selftest_wait_timeout(_stream(stream)))

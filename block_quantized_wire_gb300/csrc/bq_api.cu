@@ -50,10 +50,12 @@ namespace bqk {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxKernels = 32;
+constexpr int kMaxKernels = 64;
 std::atomic<int> g_sms[kMaxDevices];
 struct OccEntry {
     const void *kernel;
+    size_t smem;
+    int device;
     int ctas_per_sm;
 };
 OccEntry g_occ[kMaxKernels];
@@ -61,7 +63,7 @@ int g_occ_n = 0;
 std::mutex g_occ_mu;
 }  // namespace
 
-cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid)
+cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem)
 {
     int dev = 0;
     if (cudaError_t e = cudaGetDevice(&dev)) return e;
@@ -74,13 +76,18 @@ cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid)
     {
         std::lock_guard<std::mutex> lock(g_occ_mu);
         for (int i = 0; i < g_occ_n; i++)
-            if (g_occ[i].kernel == kernel) occ = g_occ[i].ctas_per_sm;
+            if (g_occ[i].kernel == kernel && g_occ[i].smem == smem && g_occ[i].device == dev) occ = g_occ[i].ctas_per_sm;
     }
     if (occ == 0) {
-        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0)) return e;
+        if (smem > 48 * 1024) {
+            if (cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(smem)))
+                return e;
+        }
+        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem)) return e;
         if (occ < 1) occ = 1;
         std::lock_guard<std::mutex> lock(g_occ_mu);
-        if (g_occ_n < kMaxKernels) g_occ[g_occ_n++] = OccEntry{kernel, occ};
+        if (g_occ_n < kMaxKernels) g_occ[g_occ_n++] = OccEntry{kernel, smem, dev, occ};
     }
     const int64_t warps_per_cta = kThreads / 32;
     const int64_t need = (nchunk + warps_per_cta - 1) / warps_per_cta;
@@ -218,5 +225,17 @@ bq_status bq_dequant_mx(const uint8_t *q_e4m3, int64_t ld_q, const uint8_t *s_e8
     return from_cuda(bqk::launch_dequant_mx(q_e4m3, ld_q, s_e8m0, ld_s, rows, cols, static_cast<uint16_t *>(out_bf16),
                                             ld_out, stream));
 }
+
+bq_status bq_take_wait_timeouts(int64_t *count)
+{
+    if (!count) return BQ_ERR_NULL;
+    unsigned long long a = 0, b = 0;
+    if (bqk::take_wait_timeouts_i8(&a) != cudaSuccess || bqk::take_wait_timeouts_mx(&b) != cudaSuccess)
+        return BQ_ERR_CUDA;
+    *count = static_cast<int64_t>(a + b);
+    return BQ_OK;
+}
+
+bq_status bq_selftest_wait_timeout(cudaStream_t stream) { return from_cuda(bqk::launch_wait_selftest(stream)); }
 
 }  // extern "C"

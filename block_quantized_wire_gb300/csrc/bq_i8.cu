@@ -101,6 +101,71 @@ __device__ __forceinline__ void run_chunks(const Op &op, int64_t nblk, int chunk
     }
 }
 
+// Staged driver: each warp keeps the inputs of its next STAGES full chunks in flight
+// as bulk copies into its own slice of shared memory (issued by lane 0, completed on
+// one mbarrier per stage), reads a chunk's inputs from shared memory into the same
+// registers the global-memory path fills, computes it exactly as that path does, and
+// then reuses the stage for the chunk STAGES ahead. Op additionally provides
+//   kStageBytes                      bytes of one chunk's staged inputs
+//   issue(c, stage, bar)             lane 0: expect_tx + bulk copies of chunk c
+//   load_staged(In&, stage pointer)  fill In from the staged copy
+// The ragged last chunk, if any, takes the global-memory path.
+template <class Op, int STAGES>
+__host__ __device__ constexpr uint32_t staged_warp_bytes()
+{
+    return 128u + STAGES * ((Op::kStageBytes + 127u) / 128u * 128u);
+}
+
+template <int STAGES, class Op>
+__device__ __forceinline__ void run_staged(const Op &op, int64_t nblk, int chunk_blocks, unsigned char *warp_smem)
+{
+    constexpr uint32_t kStride = (Op::kStageBytes + 127u) / 128u * 128u;
+    const int lane = threadIdx.x & 31;
+    const uint32_t bar0 = smem_u32(warp_smem);
+    unsigned char *buf = warp_smem + 128;
+    const uint32_t buf0 = smem_u32(buf);
+    const int64_t nfull = nblk / chunk_blocks;
+    const int64_t stride = warp_count();
+    const int64_t c0 = warp_id();
+    const int64_t K = c0 < nfull ? (nfull - c0 + stride - 1) / stride : 0;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < STAGES; st++) mbar_init(bar0 + 8 * st, 1);
+        mbar_init_fence();
+#pragma unroll
+        for (int st = 0; st < STAGES; st++)
+            if (st < K) op.issue(c0 + st * stride, buf0 + st * kStride, bar0 + 8 * st);
+    }
+    __syncwarp();
+    for (int64_t k = 0; k < K; k++) {
+        const int st = static_cast<int>(k % STAGES);
+        const uint32_t parity = static_cast<uint32_t>((k / STAGES) & 1);
+        if (!mbar_wait(bar0 + 8 * st, parity, kWaitLimitNs)) {
+            // a copy did not complete in time: record it, let the copies still in
+            // flight land (bounded) so no write reaches freed shared memory, and stop
+            if (lane == 0) atomicAdd(&g_wait_timeouts, 1ull);
+            for (int64_t j = k + 1; j < K && j < k + STAGES; j++)
+                mbar_wait(bar0 + 8 * static_cast<int>(j % STAGES), static_cast<uint32_t>((j / STAGES) & 1),
+                          kWaitLimitNs);
+            return;
+        }
+        typename Op::In in;
+        op.load_staged(in, buf + st * kStride);
+        __syncwarp();
+        if (lane == 0 && k + STAGES < K) {
+            fence_proxy_async();
+            op.issue(c0 + (k + STAGES) * stride, buf0 + st * kStride, bar0 + 8 * st);
+        }
+        op.template compute<false>(in, c0 + k * stride);
+    }
+    const int64_t c = c0 + K * stride;
+    if (c == nfull && nblk % chunk_blocks) {
+        typename Op::In t;
+        op.template load<true>(t, c);
+        op.template compute<true>(t, c);
+    }
+}
+
 // ---------------------------------------------------------------- quantize
 template <int SEGS>
 struct QuantOp {
@@ -129,6 +194,18 @@ struct QuantOp {
         for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
         requant_chunk<SEGS, kTail, false>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, nullptr);
     }
+    static constexpr uint32_t kStageBytes = 512u * SEGS;  // the chunk's BF16 values
+    static_assert(kStageBytes % 16 == 0, "bulk copies move whole 16-byte units");
+    __device__ __forceinline__ void issue(int64_t c, uint32_t stage, uint32_t bar) const
+    {
+        mbar_expect_tx(bar, kStageBytes);
+        bulk_load(stage, x + c * (256 * SEGS), kStageBytes, bar);
+    }
+    __device__ __forceinline__ void load_staged(In &in, const unsigned char *stage) const
+    {
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) in.x[j] = *reinterpret_cast<const uint4 *>(stage + 512 * j + 16 * lane);
+    }
 };
 
 template <int SEGS>
@@ -138,6 +215,16 @@ quant_i8_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict
     pdl_begin();
     const QuantOp<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
+}
+
+template <int SEGS, int STAGES>
+__global__ void __launch_bounds__(kThreads)
+quant_i8_staged_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
+{
+    pdl_begin();
+    extern __shared__ __align__(128) unsigned char smem[];
+    const QuantOp<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
+    run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<QuantOp<SEGS>, STAGES>());
 }
 
 // ---------------------------------------------------------------- materialize
@@ -252,6 +339,32 @@ struct AccumOp {
     {
         load_sources<SEGS, W, kTail>(in, src, 0, nsrc, c, nblk, lane);
     }
+    // staged inputs: the first W sources' payload runs, then their scale runs
+    static constexpr uint32_t kPayloadBytes = 256u * SEGS, kScaleBytes = 8u * SEGS;
+    static constexpr uint32_t kStageBytes = W * (kPayloadBytes + kScaleBytes);
+    static_assert(kPayloadBytes % 16 == 0 && kScaleBytes % 16 == 0 && kStageBytes % 16 == 0,
+                  "bulk copies move whole 16-byte units");
+    __device__ __forceinline__ void issue(int64_t c, uint32_t stage, uint32_t bar) const
+    {
+        mbar_expect_tx(bar, kStageBytes);
+#pragma unroll
+        for (int i = 0; i < W; i++) {
+            bulk_load(stage + i * kPayloadBytes, src.q[i] + c * (256 * SEGS), kPayloadBytes, bar);
+            bulk_load(stage + W * kPayloadBytes + i * kScaleBytes, src.s[i] + c * (2 * SEGS), kScaleBytes, bar);
+        }
+    }
+    __device__ __forceinline__ void load_staged(In &in, const unsigned char *stage) const
+    {
+#pragma unroll
+        for (int i = 0; i < W; i++) {
+#pragma unroll
+            for (int j = 0; j < SEGS; j++)
+                in.q[i][j] = *reinterpret_cast<const uint2 *>(stage + i * kPayloadBytes + 256 * j + 8 * lane);
+            in.sc[i] = lane < 2 * SEGS
+                           ? *reinterpret_cast<const float *>(stage + W * kPayloadBytes + i * kScaleBytes + 4 * lane)
+                           : 0.0f;
+        }
+    }
     template <bool kTail>
     __device__ __forceinline__ void compute(const In &in, int64_t c) const
     {
@@ -266,8 +379,24 @@ struct AccumOp {
     }
 };
 
+#ifndef BQ_ACCUM_MIN_CTAS
+#define BQ_ACCUM_MIN_CTAS 3
+#endif
+
+template <int SEGS, int W, bool kOut, int STAGES>
+__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
+accum_i8_staged_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
+                       float *__restrict__ s, uint16_t *__restrict__ out)
+{
+    pdl_begin();
+    extern __shared__ __align__(128) unsigned char smem[];
+    const AccumOp<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_staged<STAGES>(op, nblk, 2 * SEGS,
+                       smem + (threadIdx.x >> 5) * staged_warp_bytes<AccumOp<SEGS, W, kOut>, STAGES>());
+}
+
 template <int SEGS, int W, bool kOut>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
 accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s,
                 uint16_t *__restrict__ out)
 {
@@ -305,6 +434,26 @@ struct HopOp {
         in.sc = (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) ? __uint_as_float(ld_stream_u32(s_in + b0 + lane))
                                                                    : 0.0f;
     }
+    static constexpr uint32_t kQBytes = 256u * SEGS, kXBytes = 512u * SEGS, kSBytes = 8u * SEGS;
+    static constexpr uint32_t kStageBytes = kQBytes + kXBytes + kSBytes;
+    static_assert(kQBytes % 16 == 0 && kXBytes % 16 == 0 && kSBytes % 16 == 0 && kStageBytes % 16 == 0,
+                  "bulk copies move whole 16-byte units");
+    __device__ __forceinline__ void issue(int64_t c, uint32_t stage, uint32_t bar) const
+    {
+        mbar_expect_tx(bar, kStageBytes);
+        bulk_load(stage, x + c * (256 * SEGS), kXBytes, bar);
+        bulk_load(stage + kXBytes, q_in + c * (256 * SEGS), kQBytes, bar);
+        bulk_load(stage + kXBytes + kQBytes, s_in + c * (2 * SEGS), kSBytes, bar);
+    }
+    __device__ __forceinline__ void load_staged(In &in, const unsigned char *stage) const
+    {
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            in.x[j] = *reinterpret_cast<const uint4 *>(stage + 512 * j + 16 * lane);
+            in.q[j] = *reinterpret_cast<const uint2 *>(stage + kXBytes + 256 * j + 8 * lane);
+        }
+        in.sc = lane < 2 * SEGS ? *reinterpret_cast<const float *>(stage + kXBytes + kQBytes + 4 * lane) : 0.0f;
+    }
     template <bool kTail>
     __device__ __forceinline__ void compute(const In &in, int64_t c) const
     {
@@ -322,6 +471,18 @@ struct HopOp {
         requant_chunk<SEGS, kTail, kOut>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, out);
     }
 };
+
+template <int SEGS, bool kOut, int STAGES>
+__global__ void __launch_bounds__(kThreads)
+ring_hop_i8_staged_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_in,
+                          const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q,
+                          float *__restrict__ s, uint16_t *__restrict__ out)
+{
+    pdl_begin();
+    extern __shared__ __align__(128) unsigned char smem[];
+    const HopOp<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<HopOp<SEGS, kOut>, STAGES>());
+}
 
 template <int SEGS, bool kOut>
 __global__ void __launch_bounds__(kThreads)
@@ -358,10 +519,47 @@ int64_t chunks(int64_t nblk, int segs) { return (nblk + 2 * segs - 1) / (2 * seg
     if (cudaError_t e_ = grid_for((const void *)(kernel), (nchunk), &grid)) \
         return e_;
 
+// Bulk-copy stages per warp (0: the kernel reads global memory directly). Measured on
+// GB300: staging pays for the four-stream accumulate and costs for quantize.
+#ifndef BQ_STAGES_QUANT
+#define BQ_STAGES_QUANT 0
+#endif
+#ifndef BQ_STAGES_ACCUM
+#define BQ_STAGES_ACCUM 0
+#endif
+#ifndef BQ_STAGES_HOP
+#define BQ_STAGES_HOP 3
+#endif
+constexpr int kStagesQuant = BQ_STAGES_QUANT;
+constexpr int kStagesHop = BQ_STAGES_HOP;
+constexpr int kStagesAccum = BQ_STAGES_ACCUM;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Staged kernels keep STAGES bulk-copy slots per warp in dynamic shared memory.
+template <class Op, int STAGES, class Kernel, class... Args>
+cudaError_t launch_staged(Kernel kernel, int64_t nchunk, cudaStream_t st, Args... args)
+{
+    const size_t smem = (kThreads / 32) * staged_warp_bytes<Op, STAGES>();
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)kernel, nchunk, &grid, smem)) return e;
+    return launch_kernel_smem(kernel, grid, smem, st, args...);
+}
+
 template <int W, bool kOut>
 cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                            cudaStream_t st)
 {
+    if constexpr (kStagesAccum > 0) {
+        // Bulk copies need 16-byte aligned scale runs; scale pointers are only required
+        // to be 4-byte aligned, so other alignments take the global-memory path.
+        bool staged = true;
+        for (int i = 0; i < W && i < nsrc; i++) staged = staged && aligned16(src.s[i]);
+        if (staged)
+            return launch_staged<AccumOp<kSegsAccum, W, kOut>, kStagesAccum>(
+                accum_i8_staged_kernel<kSegsAccum, W, kOut, kStagesAccum>, chunks(nblk, kSegsAccum), st, src, nsrc,
+                nblk, q, s, out);
+    }
     auto kernel = accum_i8_kernel<kSegsAccum, W, kOut>;
     BQK_GRID(kernel, chunks(nblk, kSegsAccum));
     return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
@@ -369,10 +567,51 @@ cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t
 
 }  // namespace
 
-cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
+namespace {
+template <int STAGES>
+cudaError_t launch_quant_stages(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
 {
+    if constexpr (STAGES > 0)  // x is 16-byte aligned by contract
+        return launch_staged<QuantOp<kSegsQuant>, STAGES>(quant_i8_staged_kernel<kSegsQuant, STAGES>,
+                                                           chunks(nblk, kSegsQuant), st, x, nblk, q, s);
     BQK_GRID(quant_i8_kernel<kSegsQuant>, chunks(nblk, kSegsQuant));
     return launch_kernel(quant_i8_kernel<kSegsQuant>, grid, st, x, nblk, q, s);
+}
+}  // namespace
+
+cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
+{
+    return launch_quant_stages<kStagesQuant>(x, nblk, q, s, st);
+}
+
+namespace {
+// One warp waits, with a short limit, on a barrier that no thread arrives at and no
+// copy completes: the bounded wait must give up and count the timeout.
+__global__ void wait_selftest_kernel()
+{
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    const bool done = mbar_wait(b, 0, 20000000ull);  // 20 ms
+    if (!done && threadIdx.x == 0) atomicAdd(&g_wait_timeouts, 1ull);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(cudaStream_t st)
+{
+    wait_selftest_kernel<<<1, 32, 0, st>>>();
+    return cudaGetLastError();
+}
+
+cudaError_t take_wait_timeouts_i8(unsigned long long *count)
+{
+    unsigned long long zero = 0;
+    if (cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof zero)) return e;
+    return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof zero);
 }
 
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
@@ -395,16 +634,28 @@ cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *
     }
 }
 
+namespace {
+template <int STAGES, bool kOut>
+cudaError_t launch_hop_stages(const int8_t *q_in, const float *s_in, const uint16_t *x, int64_t nblk, int8_t *q,
+                              float *s, uint16_t *out, cudaStream_t st)
+{
+    if constexpr (STAGES > 0) {
+        // the incoming scales are only required to be 4-byte aligned
+        if (aligned16(s_in))
+            return launch_staged<HopOp<kSegsHop, kOut>, STAGES>(ring_hop_i8_staged_kernel<kSegsHop, kOut, STAGES>,
+                                                                 chunks(nblk, kSegsHop), st, q_in, s_in, x, nblk, q, s,
+                                                                 out);
+    }
+    BQK_GRID((ring_hop_i8_kernel<kSegsHop, kOut>), chunks(nblk, kSegsHop));
+    return launch_kernel(ring_hop_i8_kernel<kSegsHop, kOut>, grid, st, q_in, s_in, x, nblk, q, s, out);
+}
+}  // namespace
+
 cudaError_t launch_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint16_t *x, int64_t nblk, int8_t *q,
                                float *s, uint16_t *out, cudaStream_t st)
 {
-    if (out) {
-        BQK_GRID((ring_hop_i8_kernel<kSegsHop, true>), chunks(nblk, kSegsHop));
-        return launch_kernel(ring_hop_i8_kernel<kSegsHop, true>, grid, st, q_in, s_in, x, nblk, q, s, out);
-    }
-    BQK_GRID((ring_hop_i8_kernel<kSegsHop, false>), chunks(nblk, kSegsHop));
-    return launch_kernel(ring_hop_i8_kernel<kSegsHop, false>, grid, st, q_in, s_in, x, nblk, q, s,
-                         static_cast<uint16_t *>(nullptr));
+    if (out) return launch_hop_stages<kStagesHop, true>(q_in, s_in, x, nblk, q, s, out, st);
+    return launch_hop_stages<kStagesHop, false>(q_in, s_in, x, nblk, q, s, nullptr, st);
 }
 
 }  // namespace bqk

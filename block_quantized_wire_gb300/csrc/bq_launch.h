@@ -41,12 +41,12 @@ cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, 
 #endif
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, Args... args)
+cudaError_t launch_kernel_smem(void (*kernel)(KArgs...), int grid, size_t smem, cudaStream_t st, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -56,9 +56,23 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, A
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Grid size for a grid-stride kernel over `nchunk` warp chunks: enough CTAs to fill
-// every SM of the current device at the kernel's occupancy, and no more CTAs than
-// there are chunks. Returns the error of the device queries, if any.
-cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid);
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, Args... args)
+{
+    return launch_kernel_smem(kernel, grid, 0, st, args...);
+}
+
+// Grid size for a grid-stride kernel over `nchunk` warp chunks with `smem` bytes of
+// dynamic shared memory per CTA: enough CTAs to fill every SM of the current device at
+// the kernel's occupancy, and no more CTAs than there are chunks. The first call for a
+// kernel also raises its dynamic shared memory limit to `smem`. Returns the error of
+// the device queries, if any.
+cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem = 0);
+
+// Bounded waits that ran out since the last call, per translation unit (see
+// g_wait_timeouts in bq_device.cuh); each call reads and clears its unit's count.
+cudaError_t take_wait_timeouts_i8(unsigned long long *count);
+cudaError_t take_wait_timeouts_mx(unsigned long long *count);
+cudaError_t launch_wait_selftest(cudaStream_t st);
 
 }  // namespace bqk

@@ -163,6 +163,20 @@ BQ_API bq_status bq_dequant_mx(const uint8_t *q_e4m3, int64_t ld_q, const uint8_
                         int64_t ld_s, int64_t rows, int64_t cols, void *out_bf16,
                         int64_t ld_out, cudaStream_t stream);
 
+/* Number of bounded waits inside codec kernels that ran out since the previous call;
+ * the count is reset to 0. Kernels that stage their inputs through shared memory wait
+ * on hardware bulk-copy completions. A wait that has not completed within 1 s is
+ * abandoned: that warp stops early (the outputs of the chunks it had not reached are
+ * not written) and this count grows by one, instead of the kernel spinning forever.
+ * Synchronizes with the current device (the count lives in device memory).
+ *   count  host pointer receiving the number of abandoned waits. */
+BQ_API bq_status bq_take_wait_timeouts(int64_t *count);
+
+/* Self-test of the bounded wait: one warp waits on a barrier that nothing completes,
+ * with a 20 ms limit, so the count read by bq_take_wait_timeouts grows by exactly one.
+ * Enqueued on `stream`; the device stays usable afterwards. */
+BQ_API bq_status bq_selftest_wait_timeout(cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

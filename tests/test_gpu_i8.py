@@ -305,3 +305,50 @@ def test_tiny_scale_blocks_across_the_exact_division_cutoff():
     qh_r, sh_r, _ = oracle.ring_hop_i8(qz, sz, xb)
     assert_same(qh, qh_r, "hop payload")
     assert_same(sh, sh_r, "hop scales")
+
+
+def _scales_at_4_mod_16(s: np.ndarray) -> torch.Tensor:
+    buf = torch.zeros(s.size + 4, dtype=torch.float32, device="cuda")
+    view = buf[1:1 + s.size]  # 4 bytes past a 16-byte boundary
+    view.copy_(torch.from_numpy(s))
+    assert view.data_ptr() % 16 == 4
+    return view
+
+
+def test_accumulate_with_scales_not_16_byte_aligned():
+    # scale pointers only 4-byte aligned (allowed by the ABI) take the path that loads
+    # from global memory directly; payloads still 16-byte aligned
+    rng = np.random.default_rng(404)
+    nblk, W = 1027, 4
+    xs = [adversarial_blocks(rng, nblk, max_abs=1.0e37).reshape(-1) for _ in range(W)]
+    ref = [oracle.quant_i8(x) for x in xs]
+    qd, sd = [], []
+    for q, s in ref:
+        qd.append(torch.from_numpy(q).cuda())
+        sd.append(_scales_at_4_mod_16(s))
+    n = nblk * 128
+    _, qo, so = codec.empty_wire_i8(n)
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    codec.dequant_accum_i8(qd, sd, qo, so, out)
+    qa, sa, oa = oracle.dequant_accum_i8([r[0] for r in ref], [r[1] for r in ref], materialize=True)
+    assert_same(qo, qa, "payload")
+    assert_same(so, sa, "scales")
+    assert_same(out, oa, "materialized")
+
+
+def test_ring_hop_with_scales_not_16_byte_aligned():
+    # the hop stages its inputs through shared memory only when the incoming scales
+    # are 16-byte aligned; 4-byte aligned scales take the direct-load path
+    rng = np.random.default_rng(405)
+    nblk = 1029
+    x_in = adversarial_blocks(rng, nblk, max_abs=1.0e37).reshape(-1)
+    x_loc = adversarial_blocks(rng, nblk, max_abs=1.0e37).reshape(-1)
+    q_in, s_in = oracle.quant_i8(x_in)
+    n = nblk * 128
+    _, qo, so = codec.empty_wire_i8(n)
+    out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    codec.ring_hop_i8(torch.from_numpy(q_in).cuda(), _scales_at_4_mod_16(s_in), from_bits_bf16(x_loc), qo, so, out)
+    qh, sh, oh = oracle.ring_hop_i8(q_in, s_in, x_loc, materialize=True)
+    assert_same(qo, qh, "payload")
+    assert_same(so, sh, "scales")
+    assert_same(out, oh, "materialized")

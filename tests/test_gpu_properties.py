@@ -98,3 +98,20 @@ def test_error_vs_unquantized_sum_is_within_half_step_bounds():
     q, s, out = topology.i8_roundtrip(x)
     err1 = (out.double() - x.double()).abs().max().item()
     assert err1 < 0.05, err1
+
+
+def test_bounded_waits_do_not_run_out_and_can_be_observed():
+    # the staged kernels ran throughout the suite without an abandoned wait
+    codec.take_wait_timeouts()  # clear whatever earlier tests left
+    xs = [x.cuda() for x in inputs.a2a_3072(rows=3072)]
+    topology.i8_a2a(xs)
+    torch.cuda.synchronize()
+    assert codec.take_wait_timeouts() == 0
+    # a wait that nothing completes gives up after its limit and is counted; the
+    # device stays usable
+    codec.selftest_wait_timeout()
+    torch.cuda.synchronize()
+    assert codec.take_wait_timeouts() == 1
+    assert codec.take_wait_timeouts() == 0
+    q, s, out = topology.i8_roundtrip(xs[0])
+    assert torch.isfinite(out.float()).all()
