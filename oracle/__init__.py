@@ -18,6 +18,8 @@ Each function follows the pull-request pages on the wire codec:
   "feat(pcie_dma): add INT8 and MXFP8 wire modes", Summary and the review comment
   on ``mxfp8_scale_byte``; slices per "[II] Support staged MXFP8 linear inputs",
   Behavior and Compatibility.
+* ``dequant_accum_mx`` / ``ring_hop_mx``: the mx_a2a and mx_ring modes of the MXFP8
+  page's Summary, on flat MX wires (E4M3 [n] then E8M0 [n/32]).
 """
 from __future__ import annotations
 
@@ -63,6 +65,8 @@ def _load():
                 "bqo_ring_hop_i8": [P, P, P, I64, P, P, P],
                 "bqo_quant_mx": [P, I64, I64, I64, P, I64, P, I64],
                 "bqo_dequant_mx": [P, I64, P, I64, I64, I64, P, I64],
+                "bqo_dequant_accum_mx": [P, P, ctypes.c_int, I64, P, P, P],
+                "bqo_ring_hop_mx": [P, P, P, I64, P, P, P],
             }.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args
@@ -202,6 +206,62 @@ def dequant_mx(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     _check(_load().bqo_dequant_mx(_ptr(q), cols, _ptr(s), cols // GROUP_MX, rows, cols, _ptr(out), cols),
            "dequant_mx")
     return out
+
+
+def dequant_accum_mx(qs, ss, materialize: bool = True):
+    """W flat MX wires (codes uint8 [n], E8M0 uint8 [n/32]) -> (codes, E8M0, BF16 bits or None).
+
+    Decodes every source exactly to FP32, sums in source order 0..W-1 in FP32,
+    requantizes per 32-value group and (when asked) materializes the new payload.
+    """
+    W = len(qs)
+    if W != len(ss) or W < 1:
+        raise ValueError("oracle dequant_accum_mx: need W >= 1 matching sources")
+    qs = [np.ascontiguousarray(q, dtype=np.uint8).reshape(-1) for q in qs]
+    ss = [np.ascontiguousarray(s, dtype=np.uint8).reshape(-1) for s in ss]
+    n = qs[0].size
+    for q, s in zip(qs, ss):
+        if q.size != n or s.size * GROUP_MX != n:
+            raise ValueError("oracle dequant_accum_mx: sources differ in size")
+    qp = (ctypes.c_void_p * W)(*[_ptr(q) for q in qs])
+    sp = (ctypes.c_void_p * W)(*[_ptr(s) for s in ss])
+    q_out = np.empty(n, np.uint8)
+    s_out = np.empty(n // GROUP_MX, np.uint8)
+    out = np.empty(n, np.uint16) if materialize else None
+    rc = _load().bqo_dequant_accum_mx(
+        ctypes.cast(qp, ctypes.c_void_p), ctypes.cast(sp, ctypes.c_void_p), W, n,
+        _ptr(q_out), _ptr(s_out), _ptr(out) if materialize else None)
+    _check(rc, "dequant_accum_mx")
+    return q_out, s_out, out
+
+
+def ring_hop_mx(q_in, s_in, x_local_bits, materialize: bool = False):
+    """Incoming flat MX wire + local BF16 shard -> (codes, E8M0, BF16 bits or None)."""
+    q_in = np.ascontiguousarray(q_in, dtype=np.uint8).reshape(-1)
+    s_in = np.ascontiguousarray(s_in, dtype=np.uint8).reshape(-1)
+    x = np.ascontiguousarray(x_local_bits, dtype=np.uint16).reshape(-1)
+    n = q_in.size
+    if x.size != n or s_in.size * GROUP_MX != n:
+        raise ValueError("oracle ring_hop_mx: operand sizes differ")
+    q_out = np.empty(n, np.uint8)
+    s_out = np.empty(n // GROUP_MX, np.uint8)
+    out = np.empty(n, np.uint16) if materialize else None
+    rc = _load().bqo_ring_hop_mx(_ptr(q_in), _ptr(s_in), _ptr(x), n, _ptr(q_out), _ptr(s_out),
+                                 _ptr(out) if materialize else None)
+    _check(rc, "ring_hop_mx")
+    return q_out, s_out, out
+
+
+def quant_mx_flat(x_bits: np.ndarray):
+    """BF16 bits [n] -> flat MX wire (codes [n], E8M0 [n/32]); n % 128 == 0."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(1, -1)
+    q, s = quant_mx(x)
+    return q.reshape(-1), s.reshape(-1)
+
+
+def dequant_mx_flat(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """Flat MX wire -> BF16 bits [n]."""
+    return dequant_mx(np.asarray(q, np.uint8).reshape(1, -1), np.asarray(s, np.uint8).reshape(1, -1)).reshape(-1)
 
 
 # ---------------------------------------------------------------- scalar helpers (for pins)

@@ -47,7 +47,18 @@
  *       even, saturated to +-448, and the sign of zero is kept;
  *   R6  the MX value fed to E4M3 is x * 2^(127 - e), which is x divided by the
  *       group's power-of-two scale;
- *   R7  inputs are finite; results for NaN or infinity are not specified.
+ *   R7  inputs are finite; results for NaN or infinity are not specified (this
+ *       includes an E8M0 byte of 255 and a wire element whose decoded value lies
+ *       outside the binary32 range);
+ *   R11 the MX all-to-all reduction follows the INT8 one with the MX codec: each
+ *       source element is decoded to binary32 (exactly), the sources are added left
+ *       to right in source order in binary32, and the sum is requantized group by
+ *       group with the MX rules, the amax taken over the binary32 sums;
+ *   R12 the MX ring hop is v = fl(decode(q_in) * 2^(e_in - 127) + x_local),
+ *       requantized with the MX rules.
+ * [MX] Summary names the mx_a2a and mx_ring modes on the same topologies as the
+ * INT8 modes and says every mode materializes the owner shard from the payload it
+ * forwards; R11 and R12 are the plainest readings of those modes.
  */
 #include <math.h>
 #include <stddef.h>
@@ -315,6 +326,79 @@ int bqo_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_
             double v = ldexp(bqo_e4m3_decode(q[r * ld_q + c]), (int)e - 127);
             out[r * ld_out + c] = bqo_bf16_round(v);
         }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8 wire reductions ([MX] Summary: mx_a2a and mx_ring).                 */
+/* A flat MX wire of n values (n % 128 == 0) is E4M3 codes [n] followed by   */
+/* E8M0 bytes [n/32]; group g covers elements [32g, 32g + 32).               */
+/* ------------------------------------------------------------------------ */
+
+/* One wire element as binary32: decode(code) * 2^(e - 127). The exact product
+ * has at most four significant bits and magnitude >= 2^-136 (or is zero), so the
+ * conversion to binary32 is exact whenever the value is in range (reading R7). */
+static float mx_element(uint8_t code, uint8_t e)
+{
+    return (float)ldexp(bqo_e4m3_decode(code), (int)e - 127);
+}
+
+/* Requantize one group of 32 binary32 values with the rules bqo_quant_mx applies
+ * to BF16 input: E8M0 byte of the group's amax, then each value scaled exactly by
+ * 2^(127 - e) (reading R6, in double, no rounding) and encoded as E4M3. */
+static void quant_group_mx(const float *v, uint8_t *q, uint8_t *s)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < BQO_GROUP; i++) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    uint8_t e = bqo_e8m0_scale(amax);
+    *s = e;
+    for (int i = 0; i < BQO_GROUP; i++) q[i] = bqo_e4m3_encode(ldexp((double)v[i], 127 - (int)e));
+}
+
+/* mx_a2a reduction (reading R11): d_w = decode(q_w) * 2^(e_w - 127) and
+ * acc = (((d_0 + d_1) + d_2) + ...) in binary32, in source order; acc is
+ * requantized group by group. When out is not NULL it receives the
+ * materialization of the new payload (the owner's copy of what it forwards). */
+int bqo_dequant_accum_mx(const uint8_t *const *q_srcs, const uint8_t *const *s_srcs, int W, int64_t n,
+                         uint8_t *q_out, uint8_t *s_out, uint16_t *out)
+{
+    if (n < 0 || n % BQO_BLOCK || W < 1) return -1;
+    float acc[BQO_GROUP];
+    for (int64_t g = 0; g < n / BQO_GROUP; g++) {
+        for (int i = 0; i < BQO_GROUP; i++) {
+            int64_t e = g * BQO_GROUP + i;
+            float a = mx_element(q_srcs[0][e], s_srcs[0][g]);
+            for (int w = 1; w < W; w++) {
+                float d = mx_element(q_srcs[w][e], s_srcs[w][g]);
+                a = a + d;
+            }
+            acc[i] = a;
+        }
+        quant_group_mx(acc, q_out + g * BQO_GROUP, s_out + g);
+    }
+    if (out) bqo_dequant_mx(q_out, n, s_out, n / BQO_GROUP, n ? 1 : 0, n, out, n);
+    return 0;
+}
+
+/* mx_ring hop (reading R12): v = fl(decode(q_in) * 2^(e_in - 127) + x_local),
+ * requantized group by group; optional materialization of the new payload. */
+int bqo_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const uint16_t *x_local, int64_t n,
+                    uint8_t *q_out, uint8_t *s_out, uint16_t *out)
+{
+    if (n < 0 || n % BQO_BLOCK) return -1;
+    float v[BQO_GROUP];
+    for (int64_t g = 0; g < n / BQO_GROUP; g++) {
+        for (int i = 0; i < BQO_GROUP; i++) {
+            int64_t e = g * BQO_GROUP + i;
+            float d = mx_element(q_in[e], s_in[g]);
+            v[i] = d + bf16_bits_to_float(x_local[e]);
+        }
+        quant_group_mx(v, q_out + g * BQO_GROUP, s_out + g);
+    }
+    if (out) bqo_dequant_mx(q_out, n, s_out, n / BQO_GROUP, n ? 1 : 0, n, out, n);
     return 0;
 }
 

@@ -168,3 +168,39 @@ def dequant_i8(q: int, s: F) -> int:
     the product rounds to zero (s >= 0 always)."""
     p = f32(q * s)
     return bf16_bits_signed(p, q < 0 and s != 0)
+
+
+# ---- MX wire reductions, with the sign of zero tracked (binary32 values as
+# (exact value, is negative zero) pairs)
+def f32_add_signed(a, b):
+    """binary32 a + b (round to nearest even). A zero sum is -0 only when both
+    operands are -0; a nonzero exact sum of two binary32 values never rounds to 0."""
+    v = f32(a[0] + b[0])
+    neg0 = v == 0 and a[0] == 0 and b[0] == 0 and a[1] and b[1]
+    return v, neg0
+
+
+def mx_element(code: int, e: int):
+    """decode(code) * 2^(e-127) as (exact value, is negative zero)."""
+    mag = dict(_E4M3)[code & 0x7F] * F(2) ** (e - 127)
+    neg = bool(code & 0x80)
+    return (-mag if neg else mag), (neg and mag == 0)
+
+
+def quant_group_mx(vals):
+    """vals: 32 (exact binary32 value, is negative zero) pairs -> (codes, E8M0 byte)."""
+    amax = max(abs(v) for v, _ in vals)
+    e = 127 if amax == 0 else e8m0_up(f32(amax / 448))
+    codes = []
+    for v, neg0 in vals:
+        c = e4m3_nearest(v * F(2) ** (127 - e))
+        if v == 0 and neg0:
+            c = 0x80
+        codes.append(c)
+    return codes, e
+
+
+def dequant_mx(code: int, e: int) -> int:
+    """BF16 bits of decode(code) * 2^(e-127) (exact product, one rounding)."""
+    v, _ = mx_element(code, e)
+    return bf16_bits_signed(v, bool(code & 0x80))

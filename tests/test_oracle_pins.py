@@ -454,6 +454,143 @@ def test_mx_dequant_of_e4m3_relative_error_bound():
     assert np.all(np.abs(xv - dv) <= spacing / 2 * scale + bf16_half_ulp)
 
 
+# ------------------------------------------------------------------ MX wire reductions
+def _mx_sources(rnd, W, ngroups, e_lo=100, e_hi=150):
+    """Random flat MX wires: finite codes (no 0x7F/0xFF), scale bytes in [e_lo, e_hi]."""
+    qs, ss = [], []
+    finite = [c for c in range(256) if c & 0x7F != 0x7F]
+    for _ in range(W):
+        qs.append(np.array([rnd.choice(finite) for _ in range(32 * ngroups)], np.uint8))
+        ss.append(np.array([rnd.randint(e_lo, e_hi) for _ in range(ngroups)], np.uint8))
+    return qs, ss
+
+
+def test_mx_accumulate_follows_source_order_exact():
+    # mx_a2a (reading R11): d_w = decode(q_w) 2^(e_w-127) exactly, acc = ((d_0 + d_1) +
+    # d_2) + d_3 in binary32, requantized per group from the binary32 amax. Checked
+    # against exact rationals with the sign of zero tracked.
+    rnd = random.Random(11)
+    W, ng = 4, 24
+    qs, ss = _mx_sources(rnd, W, ng)
+    # group 0: big, tiny, -big, tiny (absorption makes the order visible)
+    ss[0][0], ss[1][0], ss[2][0], ss[3][0] = 150, 100, 150, 100
+    qs[0][:32] = 0x70  # 256
+    qs[2][:32] = 0xF0  # -256
+    qs[1][:32] = 0x01
+    qs[3][:32] = 0x01
+    # group 1: every source -0 except a +0 in element 0 (IEEE: -0 + -0 = -0, -0 + +0 = +0)
+    for w in range(W):
+        qs[w][32:64] = 0x80
+    qs[2][32] = 0x00
+    # group 2: all zero codes in every source (amax 0 -> byte 127)
+    for w in range(W):
+        qs[w][64:96] = 0x00
+    # group 3: scale byte 0 and small codes: decoded values down to 2^-136, below the
+    # BF16 subnormal range but exact in binary32
+    for w in range(W):
+        ss[w][3] = 0
+        qs[w][96:128] = [rnd.choice([0x01, 0x02, 0x03, 0x05, 0x09, 0x81, 0x83, 0x8A]) for _ in range(32)]
+    q_out, s_out, out = oracle.dequant_accum_mx(qs, ss)
+    for g in range(ng):
+        acc = []
+        for i in range(32):
+            e = 32 * g + i
+            a = exact.mx_element(int(qs[0][e]), int(ss[0][g]))
+            for w in range(1, W):
+                a = exact.f32_add_signed(a, exact.mx_element(int(qs[w][e]), int(ss[w][g])))
+            acc.append(a)
+        codes, eg = exact.quant_group_mx(acc)
+        assert s_out[g] == eg, g
+        assert list(q_out[32 * g:32 * g + 32]) == codes, g
+        assert [int(b) for b in out[32 * g:32 * g + 32]] == [exact.dequant_mx(c, eg) for c in codes]
+    assert s_out[2] == 127 and np.all(q_out[64:96] == 0)
+    assert q_out[32] == 0x00 and np.all(q_out[33:64] == 0x80)
+    # source order matters for group 0
+    d = [exact.mx_element(int(qs[w][0]), int(ss[w][0]))[0] for w in range(W)]
+    in_order = exact.f32(exact.f32(exact.f32(d[0] + d[1]) + d[2]) + d[3])
+    regrouped = exact.f32(exact.f32(d[0] + d[2]) + exact.f32(d[1] + d[3]))
+    assert in_order != regrouped
+    # canonical forwarding: the owner output is the materialization of the payload
+    assert np.array_equal(out, oracle.dequant_mx_flat(q_out, s_out))
+
+
+def test_mx_ring_hop_exact():
+    # mx_ring (reading R12): v = fl(decode(q_in) 2^(e_in-127) + x_local), requantized
+    rnd = random.Random(12)
+    x_in = _adversarial_blocks(rnd, 6).reshape(-1)
+    x_loc = _adversarial_blocks(rnd, 6).reshape(-1)
+    x_loc[:64] = x_in[:64] ^ 0x8000  # cancellations to exact zeros and tiny sums
+    q_in, s_in = oracle.quant_mx_flat(x_in)
+    q_out, s_out, out = oracle.ring_hop_mx(q_in, s_in, x_loc, materialize=True)
+    for g in range(x_in.size // 32):
+        v = []
+        for i in range(32):
+            e = 32 * g + i
+            xl = (exact.bits_to_value(int(x_loc[e])), int(x_loc[e]) == 0x8000)
+            v.append(exact.f32_add_signed(exact.mx_element(int(q_in[e]), int(s_in[g])), xl))
+        codes, eg = exact.quant_group_mx(v)
+        assert s_out[g] == eg, g
+        assert list(q_out[32 * g:32 * g + 32]) == codes, g
+    assert np.array_equal(out, oracle.dequant_mx_flat(q_out, s_out))
+
+
+def test_mx_single_source_accumulate_preserves_quantized_wires():
+    # For a wire quantized from BF16, each group's largest |x 2^(127-e)| exceeds 224,
+    # so its largest code is in [224, 448]. Requantizing the exact decode keeps the
+    # scale byte and every code when that code is above 224, and otherwise (largest
+    # code exactly 224) lowers the byte by one and doubles every code exactly. Either
+    # way the one-source reduction preserves every value, and the sign of zero.
+    rnd = random.Random(13)
+    x = _adversarial_blocks(rnd, 16).reshape(-1)
+    q, s = oracle.quant_mx_flat(x)
+    q1, s1, out1 = oracle.dequant_accum_mx([q], [s])
+    assert np.array_equal(out1, oracle.dequant_mx_flat(q, s))
+    cmax = (q.reshape(-1, 32) & 0x7F).max(axis=1)
+    same = cmax > 0x76  # largest magnitude above 224
+    assert np.array_equal(s1[same], s[same])
+    assert np.array_equal(q1.reshape(-1, 32)[same], q.reshape(-1, 32)[same])
+    moved = ~same & (s > 0) & (cmax > 0)
+    assert moved.any() and np.all(cmax[moved] == 0x76) and np.array_equal(s1[moved], s[moved] - 1)
+    # a hop onto +0 is the same requantization, except -0 + +0 = +0
+    zeros = np.zeros(x.size, np.uint16)
+    q2, s2, out2 = oracle.ring_hop_mx(q, s, zeros, materialize=True)
+    assert np.array_equal(s2, s1)
+    assert np.array_equal(q2, np.where(q1 == 0x80, 0, q1).astype(np.uint8))
+    assert np.array_equal(out2, np.where(out1 == 0x8000, 0, out1).astype(np.uint16))
+
+
+def test_e8m0_scale_over_fp32_amax_closed_form():
+    # The MX reductions take the scale of binary32 sums, so the scale rule is pinned
+    # over binary32 amax too: a stride through every positive finite binary32 pattern
+    # plus the powers of two and their neighbours, against the frexp closed form.
+    bits = np.concatenate([np.arange(1, 0x7F800000, 4099, dtype=np.uint32),
+                           np.array([(k << 23) + d for k in range(1, 255) for d in (-1, 0, 1)], np.uint32),
+                           np.arange(1, 64, dtype=np.uint32)])
+    a = bits.view(np.float32)
+    v = (a / np.float32(448.0)).astype(np.float32)
+    m, k = np.frexp(v.astype(np.float64))
+    expect = np.clip(np.where(v == 0, -127, np.where(m == 0.5, k - 1, k)) + 127, 0, 254)
+    got = np.array([oracle.e8m0_scale(float(t)) for t in a], np.int64)
+    assert np.array_equal(got, expect)
+
+
+def test_e4m3_encode_of_fp32_values_at_and_around_every_tie():
+    # binary32 inputs carry more bits than BF16: every midpoint between consecutive
+    # E4M3 values, its binary32 neighbours, and random binary32 values, against the
+    # nearest-value search (both signs).
+    vals = [v for _, v in exact.e4m3_values()]
+    pts = []
+    for lo, hi in zip(vals, vals[1:]):
+        mid = np.float32(float((lo + hi) / 2))
+        pts += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(1e9))]
+    rng = np.random.default_rng(14)
+    pts += list((rng.random(3000) * 470).astype(np.float32)) + list(np.float32(2.0) ** rng.uniform(-16, -8, 500).astype(np.float32))
+    for y in pts:
+        want = exact.e4m3_nearest(F(float(y)))
+        assert oracle.e4m3_encode(float(y)) == want, float(y)
+        assert oracle.e4m3_encode(-float(y)) == (want | 0x80), float(y)
+
+
 # ------------------------------------------------------------------ staged == concatenated
 def test_staged_slices_equal_concatenated():
     # "[II] Support staged MXFP8 linear inputs": quantizing 128-column-aligned slices
