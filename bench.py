@@ -62,6 +62,8 @@ def kernel_bytes(name: str, n: int) -> int:
         "ring_hop_i8": w + BF16 + w,
         "quant_mx": BF16 + w,
         "dequant_mx": w + BF16,
+        "dequant_accum_mx": W_SRC * w + w,
+        "ring_hop_mx": w + BF16 + w,
     }[name]
     return int(round(per * n))
 
@@ -328,6 +330,43 @@ def cpu_inputs(rows: int, slice_rows: int):
     return [x.cpu() for x in xs], [s.cpu() for s in sl]
 
 
+# ---------------------------------------------------------------- widened rows
+def time_next_rows(pipe, args, peak):
+    """Per-launch duration of dequant_accum_mx (W=4) and ring_hop_mx over the prefill
+    buffers as flat MX wires: CUDA events around `reps` back-to-back launches of each
+    kernel on the launching stream, after 3 warm-up launches. Every launch reads and
+    writes more than the 129 MB L2 holds, so launches do not hit in L2."""
+    c = pipe.codec
+    n = pipe.n
+    wires = [c.empty_wire_mx(n, pipe.xs[0].device) for _ in range(W_SRC + 2)]
+    for w in range(W_SRC):
+        c.quant_mx_flat(pipe.xs[w].view(-1), wires[w][1], wires[w][2])
+    acc, hop = wires[W_SRC], wires[W_SRC + 1]
+    runs = {
+        "dequant_accum_mx": lambda: c.dequant_accum_mx([wires[w][1] for w in range(W_SRC)],
+                                                       [wires[w][2] for w in range(W_SRC)], acc[1], acc[2], None),
+        "ring_hop_mx": lambda: c.ring_hop_mx(wires[0][1], wires[0][2], pipe.xs[1].view(-1), hop[1], hop[2], None),
+    }
+    out = {}
+    for name, fn in runs.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.next_reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        avg_ms = e0.elapsed_time(e1) / args.next_reps
+        nbytes = kernel_bytes(name, n)
+        gbs = nbytes / (avg_ms * 1e-3) / 1e9
+        out[name] = {"launches": args.next_reps, "avg_us": round(avg_ms * 1e3, 2), "bytes_per_launch": nbytes,
+                     "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    del wires
+    return out
+
+
 # ---------------------------------------------------------------- arms
 def run_bq(args, rank, world, local):
     from block_quantized_wire_gb300 import build as bq_build
@@ -405,6 +444,10 @@ def run_bq(args, rank, world, local):
                 else "fallback 6.8 TB/s", "unit": "GB/s", "frac": dk["frac"], "traffic": traffic,
                 "algorithmic_bytes": dk["bytes_per_launch"]}
 
+    # The MXFP8 wire reductions (mx_a2a accumulate, mx_ring hop) on the same prefill
+    # buffers: rows that widen the hot path, timed apart from the step.
+    next_rows = None if args.no_next else time_next_rows(pipe, args, peak)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -448,7 +491,7 @@ def run_bq(args, rank, world, local):
                    "step_bytes": step_bytes, "launches_per_step": nl,
                    "l2": "no flush: step working set ~12.5 GB >> 129 MB L2",
                    "parallelism": f"replicas x{world} (no collective)"},
-        "roofline": roofline, "kernels": kernels, "clocks": clocks,
+        "roofline": roofline, "kernels": kernels, "next_rows": next_rows, "clocks": clocks,
         "e2e": e2e, "gpu_launches": nl * args.steps, "cpu_baseline": cpu,
         "device": torch.cuda.get_device_name(dev),
     }
@@ -500,6 +543,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip timing the MX wire reductions")
+    ap.add_argument("--next-reps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-slice-rows", type=int, default=256)
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of CPU work for --impl reference")

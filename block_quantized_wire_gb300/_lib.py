@@ -15,6 +15,7 @@ from . import build as _build
 _lock = threading.Lock()
 _lib = None
 
+ABI_VERSION = 2
 BQ_OK = 0
 STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_ALIAS",
                 5: "BQ_ERR_CUDA"}
@@ -31,6 +32,8 @@ _PROTOS = {
     "bq_ring_hop_i8": ([_P, _P, _P, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_quant_mx": ([_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
     "bq_dequant_mx": ([_P, _I64, _P, _I64, _I64, _I64, _P, _I64, _P], ctypes.c_int),
+    "bq_dequant_accum_mx": ([_P, _P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
+    "bq_ring_hop_mx": ([_P, _P, _P, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_take_wait_timeouts": ([_P], ctypes.c_int),
     "bq_selftest_wait_timeout": ([_P], ctypes.c_int),
 }
@@ -63,8 +66,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = res
-            if lib.bq_abi_version() != 1:
-                raise ImportError(f"libbq.so ABI version {lib.bq_abi_version()} != 1")
+            if lib.bq_abi_version() != ABI_VERSION:
+                raise ImportError(f"libbq.so ABI version {lib.bq_abi_version()} != {ABI_VERSION}")
             _lib = lib
     return _lib
 

@@ -7,7 +7,9 @@ place; nothing is allocated here except by the explicit ``empty_*`` helpers.
 
 Wire layout (include/bq.h): an n-value INT8 wire is ``q`` (int8 [n]) followed by
 ``scales`` (float32 [n/128]); an MXFP8 tensor [rows, cols] is ``q`` (uint8 E4M3
-[rows, cols]) and ``s`` (uint8 E8M0 [rows, cols/32]).
+[rows, cols]) and ``s`` (uint8 E8M0 [rows, cols/32]); a flat MXFP8 wire of n values
+(the all-reduce shard of the mx_a2a / mx_ring modes) is ``q`` (uint8 [n]) followed by
+``s`` (uint8 [n/32]).
 """
 from __future__ import annotations
 
@@ -68,6 +70,13 @@ def empty_wire_i8(n: int, device="cuda"):
     q = buf[:n].view(torch.int8)
     s = buf[n:].view(torch.float32)
     return buf, q, s
+
+
+def empty_wire_mx(n: int, device="cuda"):
+    """One contiguous n-value flat MXFP8 wire buffer: (buffer, E4M3 codes [n], E8M0 [n/32])."""
+    nbytes = wire_bytes(n)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return buf, buf[:n], buf[n:]
 
 
 def empty_mx(rows: int, cols: int, device="cuda"):
@@ -155,6 +164,53 @@ def dequant_mx(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor, stream=None)
     if (sr, sc) != (rows, cols // GROUP_MX) or (orr, oc) != (rows, cols):
         raise ValueError("dequant_mx: shapes do not match")
     check("bq_dequant_mx", load().bq_dequant_mx(qp, ld_q, sp, ld_s, rows, cols, op, ld_o, _stream(stream)))
+
+
+# ---------------------------------------------------------------- flat MXFP8 wires
+def quant_mx_flat(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
+    """BF16 x [n] -> flat MX wire q [n] + s [n/32] (bq_quant_mx on one row of n values)."""
+    n = x.numel()
+    quant_mx(x.reshape(1, n), q.reshape(1, n), s.reshape(1, n // GROUP_MX), stream)
+
+
+def dequant_mx_flat(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Flat MX wire q [n] + s [n/32] -> BF16 out [n] (bq_dequant_mx on one row)."""
+    n = q.numel()
+    dequant_mx(q.reshape(1, n), s.reshape(1, n // GROUP_MX), out.reshape(1, n), stream)
+
+
+def dequant_accum_mx(q_srcs: Sequence[torch.Tensor], s_srcs: Sequence[torch.Tensor], q_out: torch.Tensor,
+                     s_out: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Sum W decoded flat MX wires in FP32 in list order, requantize into q_out/s_out;
+    optionally materialize the new wire into out (BF16)."""
+    W = len(q_srcs)
+    if W != len(s_srcs):
+        raise ValueError("dequant_accum_mx: q_srcs and s_srcs differ in length")
+    n = q_out.numel()
+    for q, sc in zip(q_srcs, s_srcs):
+        if q.numel() != n or sc.numel() * GROUP_MX != n:
+            raise ValueError("dequant_accum_mx: a source's size differs from the output's")
+    if s_out.numel() * GROUP_MX != n or (out is not None and out.numel() != n):
+        raise ValueError("dequant_accum_mx: output sizes do not match")
+    qp = (ctypes.c_void_p * max(W, 1))(*[_flat(q, torch.uint8, "q_srcs[]") for q in q_srcs])
+    sp = (ctypes.c_void_p * max(W, 1))(*[_flat(sc, torch.uint8, "s_srcs[]") for sc in s_srcs])
+    check("bq_dequant_accum_mx", load().bq_dequant_accum_mx(
+        ctypes.cast(qp, ctypes.c_void_p), ctypes.cast(sp, ctypes.c_void_p), W, n,
+        _flat(q_out, torch.uint8, "q_out"), _flat(s_out, torch.uint8, "s_out"),
+        _flat(out, torch.bfloat16, "out") if out is not None else None, _stream(stream)))
+
+
+def ring_hop_mx(q_in: torch.Tensor, s_in: torch.Tensor, x_local: torch.Tensor, q_out: torch.Tensor,
+                s_out: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Fused MX hop: decode(q_in, s_in) + x_local in FP32, requantized into q_out/s_out."""
+    n = q_in.numel()
+    if (x_local.numel() != n or q_out.numel() != n or s_in.numel() * GROUP_MX != n
+            or s_out.numel() * GROUP_MX != n or (out is not None and out.numel() != n)):
+        raise ValueError("ring_hop_mx: sizes do not match")
+    check("bq_ring_hop_mx", load().bq_ring_hop_mx(
+        _flat(q_in, torch.uint8, "q_in"), _flat(s_in, torch.uint8, "s_in"), _flat(x_local, torch.bfloat16, "x_local"),
+        n, _flat(q_out, torch.uint8, "q_out"), _flat(s_out, torch.uint8, "s_out"),
+        _flat(out, torch.bfloat16, "out") if out is not None else None, _stream(stream)))
 
 
 # ---------------------------------------------------------------- bounded waits

@@ -226,6 +226,54 @@ bq_status bq_dequant_mx(const uint8_t *q_e4m3, int64_t ld_q, const uint8_t *s_e8
                                             ld_out, stream));
 }
 
+bq_status bq_dequant_accum_mx(const uint8_t *const *q_srcs, const uint8_t *const *s_srcs, int W, int64_t n,
+                              uint8_t *q_out, uint8_t *s_out, void *out_bf16, cudaStream_t stream)
+{
+    if (W < 1 || W > BQ_MAX_W) return BQ_ERR_SHAPE;
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!q_srcs || !s_srcs || !q_out || !s_out) return BQ_ERR_NULL;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    bqk::MxSourceList src = {};
+    Range ins[2 * BQ_MAX_W];
+    for (int w = 0; w < W; w++) {
+        if (!q_srcs[w] || !s_srcs[w]) return BQ_ERR_NULL;
+        if (!aligned(q_srcs[w], 16) || !aligned(s_srcs[w], 4)) return BQ_ERR_ALIGN;
+        src.q[w] = q_srcs[w];
+        src.s[w] = reinterpret_cast<const uint32_t *>(s_srcs[w]);
+        ins[2 * w] = span(q_srcs[w], n);
+        ins[2 * w + 1] = span(s_srcs[w], 4 * nblk);
+    }
+    if (!aligned(q_out, 16) || !aligned(s_out, 4) || (out_bf16 && !aligned(out_bf16, 16))) return BQ_ERR_ALIGN;
+    Range outs[3] = {span(q_out, n), span(s_out, 4 * nblk), {}};
+    int n_out = 2;
+    if (out_bf16) outs[n_out++] = span(out_bf16, 2 * n);
+    if (any_alias(outs, n_out, ins, 2 * W)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_accum_mx(src, W, nblk, q_out, reinterpret_cast<uint32_t *>(s_out),
+                                          static_cast<uint16_t *>(out_bf16), stream));
+}
+
+bq_status bq_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const void *x_local_bf16, int64_t n,
+                         uint8_t *q_out, uint8_t *s_out, void *out_bf16, cudaStream_t stream)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!q_in || !s_in || !x_local_bf16 || !q_out || !s_out) return BQ_ERR_NULL;
+    if (!aligned(q_in, 16) || !aligned(s_in, 4) || !aligned(x_local_bf16, 16) || !aligned(q_out, 16) ||
+        !aligned(s_out, 4) || (out_bf16 && !aligned(out_bf16, 16)))
+        return BQ_ERR_ALIGN;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    const Range ins[] = {span(q_in, n), span(s_in, 4 * nblk), span(x_local_bf16, 2 * n)};
+    Range outs[3] = {span(q_out, n), span(s_out, 4 * nblk), {}};
+    int n_out = 2;
+    if (out_bf16) outs[n_out++] = span(out_bf16, 2 * n);
+    if (any_alias(outs, n_out, ins, 3)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_ring_hop_mx(q_in, reinterpret_cast<const uint32_t *>(s_in),
+                                             static_cast<const uint16_t *>(x_local_bf16), nblk, q_out,
+                                             reinterpret_cast<uint32_t *>(s_out), static_cast<uint16_t *>(out_bf16),
+                                             stream));
+}
+
 bq_status bq_take_wait_timeouts(int64_t *count)
 {
     if (!count) return BQ_ERR_NULL;

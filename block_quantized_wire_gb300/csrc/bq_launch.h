@@ -11,10 +11,15 @@ namespace bqk {
 constexpr int kThreads = 256;  // threads per CTA (8 warps) for every codec kernel
 constexpr int kMaxSources = 16;
 
-struct SourceList {
-    const int8_t *q[kMaxSources];
-    const float *s[kMaxSources];
+// The sources of a wire reduction: payload pointers and 4-byte scale-word pointers
+// (one word per 128-value block), in accumulation order.
+template <class TQ, class TS>
+struct WireList {
+    const TQ *q[kMaxSources];
+    const TS *s[kMaxSources];
 };
+using SourceList = WireList<int8_t, float>;       // block INT8: one FP32 scale per block
+using MxSourceList = WireList<uint8_t, uint32_t>;  // MXFP8: four E8M0 bytes per block
 
 cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st);
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out,
@@ -28,6 +33,10 @@ cudaError_t launch_quant_mx(const uint16_t *x, int64_t ld_x, int64_t rows, int64
 cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_s,
                               int64_t rows, int64_t cols, uint16_t *out, int64_t ld_out,
                               cudaStream_t st);
+cudaError_t launch_accum_mx(const MxSourceList &src, int W, int64_t nblk, uint8_t *q, uint32_t *s,
+                            uint16_t *out, cudaStream_t st);
+cudaError_t launch_ring_hop_mx(const uint8_t *q_in, const uint32_t *s_in, const uint16_t *x, int64_t nblk,
+                               uint8_t *q, uint32_t *s, uint16_t *out, cudaStream_t st);
 
 // Programmatic dependent launch: every codec kernel is launched with programmatic
 // stream serialization and begins with griddepcontrol.wait, which returns once the

@@ -227,13 +227,6 @@ cudaError_t launch_quant_mx(const uint16_t *x, int64_t ld_x, int64_t rows, int64
     return launch_kernel(quant_mx_kernel, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
 }
 
-cudaError_t take_wait_timeouts_mx(unsigned long long *count)
-{
-    unsigned long long zero = 0;
-    if (cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof zero)) return e;
-    return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof zero);
-}
-
 cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_s, int64_t rows,
                               int64_t cols, uint16_t *out, int64_t ld_out, cudaStream_t st)
 {

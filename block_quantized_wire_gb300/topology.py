@@ -1,4 +1,4 @@
-"""The pages' three INT8 wire topologies, simulated on one GPU.
+"""The pages' wire topologies, simulated on one GPU, for both codecs.
 
 W "ranks" are W buffers resident in one GPU's memory; moving a payload from one rank
 to another is handing over the same device tensor, so there is no transport and no
@@ -11,39 +11,55 @@ trip of one shard), ``i8_ring`` (INT8 reduce-scatter ring: the fused hop at ever
 step, then an INT8 all-gather), ``i8_a2a`` (each rank quantizes once, the shard owner
 accumulates all sources in FP32 and requantizes, then an INT8 broadcast); in every
 topology the owner materializes from the same final payload it forwards.
+
+From "feat(pcie_dma): add INT8 and MXFP8 wire modes", Summary: ``mx``, ``mx_ring`` and
+``mx_a2a`` are the same topologies with the MXFP8 codec on flat MX wires.
 """
 from __future__ import annotations
 
-from typing import List, Sequence
+from typing import Callable, List, NamedTuple, Sequence
 
 import torch
 
 from . import codec
 
 
-def i8_roundtrip(x: torch.Tensor, stream=None):
+class Wire(NamedTuple):
+    """The codec calls one topology needs, on flat wires of n values."""
+    empty: Callable
+    quant: Callable
+    dequant: Callable
+    accum: Callable
+    hop: Callable
+
+
+I8 = Wire(codec.empty_wire_i8, codec.quant_i8, codec.dequant_i8, codec.dequant_accum_i8, codec.ring_hop_i8)
+MX = Wire(codec.empty_wire_mx, codec.quant_mx_flat, codec.dequant_mx_flat, codec.dequant_accum_mx, codec.ring_hop_mx)
+
+
+def roundtrip(wire: Wire, x: torch.Tensor, stream=None):
     """Quantize one BF16 tensor and materialize it: (payload, scales, BF16)."""
     n = x.numel()
-    _, q, s = codec.empty_wire_i8(n, x.device)
+    _, q, s = wire.empty(n, x.device)
     out = torch.empty_like(x)
-    codec.quant_i8(x, q, s, stream)
-    codec.dequant_i8(q, s, out, stream)
+    wire.quant(x, q, s, stream)
+    wire.dequant(q, s, out, stream)
     return q, s, out
 
 
-def i8_a2a(xs: Sequence[torch.Tensor], stream=None):
+def a2a(wire: Wire, xs: Sequence[torch.Tensor], stream=None):
     """Quantize-once all-to-all for one owner: every source is quantized, the owner sums
     the W payloads in source order and requantizes (the broadcast payload), and
     materializes it. Returns (payload, scales, owner BF16, per-source payloads)."""
     n = xs[0].numel()
     srcs = []
     for x in xs:
-        _, q, s = codec.empty_wire_i8(n, x.device)
-        codec.quant_i8(x, q, s, stream)
+        _, q, s = wire.empty(n, x.device)
+        wire.quant(x, q, s, stream)
         srcs.append((q, s))
-    _, q_out, s_out = codec.empty_wire_i8(n, xs[0].device)
+    _, q_out, s_out = wire.empty(n, xs[0].device)
     owner = torch.empty_like(xs[0])
-    codec.dequant_accum_i8([q for q, _ in srcs], [s for _, s in srcs], q_out, s_out, owner, stream)
+    wire.accum([q for q, _ in srcs], [s for _, s in srcs], q_out, s_out, owner, stream)
     return q_out, s_out, owner, srcs
 
 
@@ -54,8 +70,8 @@ def ring_order(shard: int, W: int) -> List[int]:
     return [(shard + 1 + k) % W for k in range(W)]
 
 
-def i8_ring(xs: Sequence[torch.Tensor], stream=None):
-    """INT8 reduce-scatter ring + INT8 all-gather over W rank buffers.
+def ring(wire: Wire, xs: Sequence[torch.Tensor], stream=None):
+    """Quantized reduce-scatter ring + quantized all-gather over W rank buffers.
 
     Every buffer [rows, cols] is split into W contiguous row shards. For shard c the
     chain of ring_order(c, W) runs one quantize and W-1 fused hops, the last (at the
@@ -66,20 +82,20 @@ def i8_ring(xs: Sequence[torch.Tensor], stream=None):
     W = len(xs)
     rows = xs[0].shape[0]
     if rows % W:
-        raise ValueError("i8_ring: rows must divide evenly into W shards")
+        raise ValueError("ring: rows must divide evenly into W shards")
     shard_rows = rows // W
     shards = [[x[c * shard_rows:(c + 1) * shard_rows] for c in range(W)] for x in xs]
     n = shards[0][0].numel()
     finals, owners = [], []
     for c in range(W):
         chain = ring_order(c, W)
-        _, q, s = codec.empty_wire_i8(n, xs[0].device)
-        codec.quant_i8(shards[chain[0]][c], q, s, stream)
+        _, q, s = wire.empty(n, xs[0].device)
+        wire.quant(shards[chain[0]][c], q, s, stream)
         owner = torch.empty_like(shards[0][c])
         for step, rank in enumerate(chain[1:], start=1):
-            _, q2, s2 = codec.empty_wire_i8(n, xs[0].device)
+            _, q2, s2 = wire.empty(n, xs[0].device)
             last = step == W - 1
-            codec.ring_hop_i8(q, s, shards[rank][c], q2, s2, owner if last else None, stream)
+            wire.hop(q, s, shards[rank][c], q2, s2, owner if last else None, stream)
             q, s = q2, s2
         finals.append((q, s))
         owners.append(owner)
@@ -87,6 +103,31 @@ def i8_ring(xs: Sequence[torch.Tensor], stream=None):
     for _rank in range(W):
         out = torch.empty_like(xs[0])
         for c in range(W):
-            codec.dequant_i8(finals[c][0], finals[c][1], out[c * shard_rows:(c + 1) * shard_rows], stream)
+            wire.dequant(finals[c][0], finals[c][1], out[c * shard_rows:(c + 1) * shard_rows], stream)
         outs.append(out)
     return outs, finals, owners
+
+
+# the pages' mode names
+def i8_roundtrip(x, stream=None):
+    return roundtrip(I8, x, stream)
+
+
+def i8_a2a(xs, stream=None):
+    return a2a(I8, xs, stream)
+
+
+def i8_ring(xs, stream=None):
+    return ring(I8, xs, stream)
+
+
+def mx_roundtrip(x, stream=None):
+    return roundtrip(MX, x, stream)
+
+
+def mx_a2a(xs, stream=None):
+    return a2a(MX, xs, stream)
+
+
+def mx_ring(xs, stream=None):
+    return ring(MX, xs, stream)

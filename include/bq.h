@@ -20,6 +20,9 @@
  *                                         s[r][g] covers columns [32g, 32g+32)
  * A caller that wants one contiguous wire buffer places the scale region directly
  * after the payload region (byte offset n, which keeps 16-byte alignment).
+ * A flat MX wire (the all-reduce shard of the mx_a2a and mx_ring modes) is the
+ * one-row case: codes q[n], then E8M0 bytes s[n/32]; the four scale bytes of a
+ * 128-value block form one 4-byte word, as the INT8 scale of that block does.
  *
  * Arithmetic (bit-exact; no fused multiply-add anywhere):
  *   quantize   amax = max |x| over the block; s = fl(amax / 127) (IEEE binary32
@@ -36,6 +39,14 @@
  *              saturating).
  *   MX values  code = E4M3_rne_satfinite(x * 2^(127-e)); the sign of zero is kept.
  *   MX materialize  out = BF16_rne(decode(code) * 2^(e-127)) (the product is exact).
+ *   MX accumulate   d_w = decode(code_w) * 2^(e_w-127) (exact in binary32);
+ *              acc = (((d_0 + d_1) + d_2) + ...) in binary32 in source order; acc is
+ *              requantized per 32-value group with the MX scale and value rules,
+ *              the amax taken over the binary32 sums.
+ *   MX ring hop  v = fl(decode(code_in) * 2^(e_in-127) + x_local), requantized as
+ *              MX. (The MXFP8 page's Summary runs its codec on the same ring and
+ *              all-to-all topologies, mx_ring and mx_a2a; these two rules are the
+ *              INT8 ones with the MX codec.)
  * Inputs must be finite; results for NaN or infinity inputs are not specified.
  *
  * Conventions shared by every call:
@@ -78,7 +89,7 @@ extern "C" {
 #define BQ_API
 #endif
 
-#define BQ_ABI_VERSION 1
+#define BQ_ABI_VERSION 2
 #define BQ_BLOCK_I8 128 /* values per INT8 block */
 #define BQ_GROUP_MX 32  /* values per E8M0 scale */
 #define BQ_MAX_W 16     /* most sources one accumulate call takes */
@@ -162,6 +173,33 @@ BQ_API bq_status bq_quant_mx(const void *x_bf16, int64_t rows, int64_t cols, int
 BQ_API bq_status bq_dequant_mx(const uint8_t *q_e4m3, int64_t ld_q, const uint8_t *s_e8m0,
                         int64_t ld_s, int64_t rows, int64_t cols, void *out_bf16,
                         int64_t ld_out, cudaStream_t stream);
+
+/* mx_a2a reduction on flat MX wires: decode every source exactly to binary32, add the
+ * sources in source order in binary32, requantize per 32-value group ("feat(pcie_dma):
+ * add INT8 and MXFP8 wire modes", Summary: mx_a2a on the all-to-all topology; the
+ * owner materializes the payload it forwards).
+ *   q_srcs, s_srcs      HOST arrays of W DEVICE pointers: [n] E4M3 codes (16-byte
+ *                       aligned) and [n/32] E8M0 bytes (4-byte aligned) each; their
+ *                       order is the summation order
+ *   W                   1 <= W <= BQ_MAX_W
+ *   q_out [n], s_out [n/32]  the requantized wire (written; same alignment)
+ *   out_bf16            NULL, or [n] BF16 (16-byte aligned) receiving the
+ *                       materialization of the new wire, bit-identical to
+ *                       bq_dequant_mx(q_out, n, s_out, n/32, 1, n, out_bf16, n).
+ * Sources may repeat or overlap one another. */
+BQ_API bq_status bq_dequant_accum_mx(const uint8_t *const *q_srcs, const uint8_t *const *s_srcs,
+                              int W, int64_t n, uint8_t *q_out, uint8_t *s_out, void *out_bf16,
+                              cudaStream_t stream);
+
+/* mx_ring hop on flat MX wires: decode the incoming wire, add the local BF16 shard in
+ * binary32, requantize per 32-value group (same page, Summary: mx_ring).
+ *   q_in [n], s_in [n/32]   incoming wire (read; 16- and 4-byte aligned)
+ *   x_local_bf16 [n]        this rank's shard (read; 16-byte aligned)
+ *   q_out, s_out            outgoing wire (written)
+ *   out_bf16                NULL, or [n] BF16 materialization of the outgoing wire. */
+BQ_API bq_status bq_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const void *x_local_bf16,
+                         int64_t n, uint8_t *q_out, uint8_t *s_out, void *out_bf16,
+                         cudaStream_t stream);
 
 /* Number of bounded waits inside codec kernels that ran out since the previous call;
  * the count is reset to 0. Kernels that stage their inputs through shared memory wait

@@ -26,14 +26,15 @@ def declared_functions():
 def test_header_declares_the_calls():
     names = declared_functions()
     for want in ("bq_quant_i8", "bq_dequant_i8", "bq_dequant_accum_i8", "bq_ring_hop_i8", "bq_quant_mx",
-                 "bq_dequant_mx", "bq_wire_bytes", "bq_status_string", "bq_abi_version"):
+                 "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_wire_bytes", "bq_status_string",
+                 "bq_abi_version", "bq_take_wait_timeouts", "bq_selftest_wait_timeout"):
         assert want in names
 
 
 def test_library_exports_every_declared_symbol(bq_lib):
     for name in declared_functions():
         assert hasattr(bq_lib, name), name
-    assert bq_lib.bq_abi_version() == 1
+    assert bq_lib.bq_abi_version() == 2
 
 
 def test_wire_bytes_and_status_strings(bq_lib):
@@ -112,6 +113,45 @@ def test_ring_hop_rejections(bq_lib):
     assert f(qi, si + 2, x, n, qo, so, None, None) == ALIGN
     assert f(qi, si, x, n, x + 16, so, None, None) == ALIAS
     assert f(qi, si, x, n, qo, so, qi, None) == ALIAS
+
+
+def test_accum_mx_rejections(bq_lib):
+    f = bq_lib.bq_dequant_accum_mx
+    n = 4096
+    q = [A + k * 0x100000 for k in range(4)]
+    s = [A + 0x1000000 + k * 0x10000 for k in range(4)]
+    qp, qa = _srcs(q)
+    sp, sa = _srcs(s)
+    out_q, out_s, out_b = A + 0x2000000, A + 0x3000000, A + 0x4000000
+    assert f(qp, sp, 0, n, out_q, out_s, None, None) == SHAPE
+    assert f(qp, sp, 17, n, out_q, out_s, None, None) == SHAPE
+    assert f(qp, sp, 4, n + 32, out_q, out_s, None, None) == SHAPE  # groups of 32 but not blocks of 128
+    assert f(qp, sp, 4, 0, out_q, out_s, None, None) == OK
+    assert f(qp, None, 4, n, out_q, out_s, None, None) == NULL
+    sn, sna = _srcs([s[0], s[1], None, s[3]])
+    assert f(qp, sn, 4, n, out_q, out_s, None, None) == NULL
+    sm, sma = _srcs([s[0], s[1] + 2, s[2], s[3]])
+    assert f(qp, sm, 4, n, out_q, out_s, None, None) == ALIGN  # scale words are 4-byte aligned
+    assert f(qp, sp, 4, n, out_q + 8, out_s, None, None) == ALIGN
+    assert f(qp, sp, 4, n, out_q, out_s + 1, None, None) == ALIGN
+    assert f(qp, sp, 4, n, q[1], out_s, None, None) == ALIAS
+    assert f(qp, sp, 4, n, out_q, s[0] + 64, None, None) == ALIAS  # E8M0 run spans n/32 bytes
+    assert f(qp, sp, 4, n, out_q, out_s, out_s - 64, None) == ALIAS
+
+
+def test_ring_hop_mx_rejections(bq_lib):
+    f = bq_lib.bq_ring_hop_mx
+    n = 4096
+    qi, si, x, qo, so, ob = (A + k * 0x100000 for k in range(6))
+    assert f(qi, si, x, 160, qo, so, None, None) == SHAPE
+    assert f(qi, si, x, 0, qo, so, None, None) == OK
+    assert f(qi, None, x, n, qo, so, None, None) == NULL
+    assert f(qi, si + 1, x, n, qo, so, None, None) == ALIGN
+    assert f(qi, si, x + 8, n, qo, so, None, None) == ALIGN
+    assert f(qi, si, x, n, qo, so, ob + 2, None) == ALIGN
+    assert f(qi, si, x, n, x + 2 * n - 16, so, None, None) == ALIAS
+    assert f(qi, si, x, n, qo, si + n // 32 - 4, None, None) == ALIAS
+    assert f(qi, si, x, n, qo, so, qo + n - 16, None) == ALIAS
 
 
 def test_mx_rejections(bq_lib):
