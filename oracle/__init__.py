@@ -20,6 +20,13 @@ Each function follows the pull-request pages on the wire codec:
   Behavior and Compatibility.
 * ``dequant_accum_mx`` / ``ring_hop_mx``: the mx_a2a and mx_ring modes of the MXFP8
   page's Summary, on flat MX wires (E4M3 [n] then E8M0 [n/32]).
+* ``quant_mx(..., fmt="f16")``: FP16 slices, "[II] Support staged MXFP8 linear
+  inputs", Behavior.
+* ``reduce_quant_i8`` / ``reduce_quant_e4m3``: the BF16 reduce-scatter of the i8 mode
+  (and of the E4M3 all-gather mode) fused with its all-gather payload, block-INT8
+  page, Summary.
+* ``quant_e4m3`` / ``dequant_e4m3``: the legacy E4M3 codec the block-INT8 page
+  compares against (Summary and Why: one E4M3 byte per value, FP32 scale per 128).
 """
 from __future__ import annotations
 
@@ -67,6 +74,11 @@ def _load():
                 "bqo_dequant_mx": [P, I64, P, I64, I64, I64, P, I64],
                 "bqo_dequant_accum_mx": [P, P, ctypes.c_int, I64, P, P, P],
                 "bqo_ring_hop_mx": [P, P, P, I64, P, P, P],
+                "bqo_quant_mx_f16": [P, I64, I64, I64, P, I64, P, I64],
+                "bqo_reduce_quant_i8": [P, ctypes.c_int, I64, P, P, P],
+                "bqo_reduce_quant_e4m3": [P, ctypes.c_int, I64, P, P, P],
+                "bqo_quant_e4m3": [P, I64, P, P],
+                "bqo_dequant_e4m3": [P, P, I64, P],
             }.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args
@@ -79,6 +91,8 @@ def _load():
             lib.bqo_e4m3_decode.restype = ctypes.c_double
             lib.bqo_e8m0_scale.argtypes = [ctypes.c_float]
             lib.bqo_e8m0_scale.restype = ctypes.c_uint8
+            lib.bqo_f16_to_float.argtypes = [ctypes.c_uint16]
+            lib.bqo_f16_to_float.restype = ctypes.c_float
             lib.bqo_wire_bytes.argtypes = [I64]
             lib.bqo_wire_bytes.restype = I64
             _lib = lib
@@ -167,18 +181,23 @@ def ring_hop_i8(q_in, s_in, x_local_bits, materialize: bool = False):
 
 
 # ---------------------------------------------------------------- MXFP8
-def quant_mx(x_bits: np.ndarray):
-    """BF16 bits [rows, cols] -> (E4M3 codes [rows, cols], E8M0 bytes [rows, cols/32])."""
+def _quant_mx_fn(fmt: str):
+    if fmt not in ("bf16", "f16"):
+        raise ValueError(f"oracle quant_mx: input format {fmt!r} is not bf16 or f16")
+    return _load().bqo_quant_mx if fmt == "bf16" else _load().bqo_quant_mx_f16
+
+
+def quant_mx(x_bits: np.ndarray, fmt: str = "bf16"):
+    """BF16 (or FP16) bits [rows, cols] -> (E4M3 codes [rows, cols], E8M0 bytes [rows, cols/32])."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
     rows, cols = x.shape
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // GROUP_MX), np.uint8)
-    _check(_load().bqo_quant_mx(_ptr(x), rows, cols, cols, _ptr(q), cols, _ptr(s), cols // GROUP_MX),
-           "quant_mx")
+    _check(_quant_mx_fn(fmt)(_ptr(x), rows, cols, cols, _ptr(q), cols, _ptr(s), cols // GROUP_MX), "quant_mx")
     return q, s
 
 
-def quant_mx_into(x_bits: np.ndarray, q_buf: np.ndarray, s_buf: np.ndarray, col0: int) -> None:
+def quant_mx_into(x_bits: np.ndarray, q_buf: np.ndarray, s_buf: np.ndarray, col0: int, fmt: str = "bf16") -> None:
     """Quantize a [rows, cols] slice into columns [col0, col0+cols) of wider buffers.
 
     ``q_buf`` is uint8 [rows, C], ``s_buf`` uint8 [rows, C/32]; col0 % 128 == 0.
@@ -190,8 +209,8 @@ def quant_mx_into(x_bits: np.ndarray, q_buf: np.ndarray, s_buf: np.ndarray, col0
     assert q_buf.flags["C_CONTIGUOUS"] and s_buf.flags["C_CONTIGUOUS"]
     ld_q = q_buf.shape[1]
     ld_s = s_buf.shape[1]
-    rc = _load().bqo_quant_mx(_ptr(x), rows, cols, cols, q_buf.ctypes.data + col0, ld_q,
-                              s_buf.ctypes.data + col0 // GROUP_MX, ld_s)
+    rc = _quant_mx_fn(fmt)(_ptr(x), rows, cols, cols, q_buf.ctypes.data + col0, ld_q,
+                           s_buf.ctypes.data + col0 // GROUP_MX, ld_s)
     _check(rc, "quant_mx_into")
 
 
@@ -264,7 +283,59 @@ def dequant_mx_flat(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return dequant_mx(np.asarray(q, np.uint8).reshape(1, -1), np.asarray(s, np.uint8).reshape(1, -1)).reshape(-1)
 
 
+# ---------------------------------------------------------------- BF16 reduce + quantize, legacy E4M3
+def _reduce_quant(fn, what, x_srcs, materialize, qtype):
+    W = len(x_srcs)
+    if W < 1:
+        raise ValueError(f"oracle {what}: need W >= 1 sources")
+    xs = [np.ascontiguousarray(x, dtype=np.uint16).reshape(-1) for x in x_srcs]
+    n = xs[0].size
+    if any(x.size != n for x in xs):
+        raise ValueError(f"oracle {what}: sources differ in size")
+    xp = (ctypes.c_void_p * W)(*[_ptr(x) for x in xs])
+    q = np.empty(n, qtype)
+    s = np.empty(n // BLOCK_I8 if n % BLOCK_I8 == 0 else 0, np.float32)
+    out = np.empty(n, np.uint16) if materialize else None
+    _check(fn(ctypes.cast(xp, ctypes.c_void_p), W, n, _ptr(q), _ptr(s), _ptr(out) if materialize else None), what)
+    return q, s, out
+
+
+def reduce_quant_i8(x_srcs, materialize: bool = False):
+    """W BF16 shards -> (payload, scales, BF16 bits or None): binary32 sum in rank
+    order, rounded once to BF16, then quant_i8."""
+    return _reduce_quant(_load().bqo_reduce_quant_i8, "reduce_quant_i8", x_srcs, materialize, np.int8)
+
+
+def reduce_quant_e4m3(x_srcs, materialize: bool = False):
+    """As reduce_quant_i8 with the legacy E4M3 codec."""
+    return _reduce_quant(_load().bqo_reduce_quant_e4m3, "reduce_quant_e4m3", x_srcs, materialize, np.uint8)
+
+
+def quant_e4m3(x_bits: np.ndarray):
+    """BF16 bits [n] -> (E4M3 codes uint8 [n], scales float32 [n/128])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16).reshape(-1)
+    n = x.size
+    q = np.empty(n, np.uint8)
+    s = np.empty(n // BLOCK_I8 if n % BLOCK_I8 == 0 else 0, np.float32)
+    _check(_load().bqo_quant_e4m3(_ptr(x), n, _ptr(q), _ptr(s)), "quant_e4m3")
+    return q, s
+
+
+def dequant_e4m3(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """E4M3 codes [n] + scales [n/128] -> BF16 bits [n]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8).reshape(-1)
+    s = np.ascontiguousarray(s, dtype=np.float32).reshape(-1)
+    if s.size * BLOCK_I8 != q.size:
+        raise ValueError("oracle dequant_e4m3: scale count does not match payload")
+    out = np.empty(q.size, np.uint16)
+    _check(_load().bqo_dequant_e4m3(_ptr(q), _ptr(s), q.size, _ptr(out)), "dequant_e4m3")
+    return out
+
+
 # ---------------------------------------------------------------- scalar helpers (for pins)
+def f16_to_float(bits: int) -> float:
+    return float(_load().bqo_f16_to_float(int(bits)))
+
 def bf16_round(v: float) -> int:
     """Round a real (given exactly as a double) to a BF16 bit pattern, ties to even."""
     return int(_load().bqo_bf16_round(float(v)))

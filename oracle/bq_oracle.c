@@ -59,6 +59,18 @@
  * [MX] Summary names the mx_a2a and mx_ring modes on the same topologies as the
  * INT8 modes and says every mode materializes the owner shard from the payload it
  * forwards; R11 and R12 are the plainest readings of those modes.
+ *   R13 the i8 mode's BF16 reduce-scatter ([I8] Summary: "i8" is a BF16
+ *       reduce-scatter followed by an INT8 all-gather) sums the W ranks' BF16 shards
+ *       left to right in rank order in binary32 and rounds the sum once to BF16 (the
+ *       reduce-scatter's BF16 result); the all-gather payload is quant_i8 of that
+ *       BF16 shard, and the owner materializes that payload;
+ *   R14 the legacy E4M3 codec ([I8] Summary and Why: one E4M3 byte per value and one
+ *       FP32 scale per 128-value block, 132 bytes per block) quantizes like block INT8
+ *       with 448 in place of 127: s = fl(amax / 448), code = E4M3 (nearest, ties to
+ *       even, saturated) of fl(x / s); a block with s == 0 has every code 0x00;
+ *       materialization is BF16(fl(decode(code) * s));
+ *   R15 an FP16 slice ([ST] Behavior: BF16 or FP16 feature slices) is widened
+ *       exactly to binary32 and quantized with the MX rules unchanged.
  */
 #include <math.h>
 #include <stddef.h>
@@ -114,6 +126,21 @@ uint16_t bqo_bf16_round(double v)
     else if (above < below) pick = up;
     else pick = (lo % 2 == 0) ? lo : up;   /* tie: even code */
     return (uint16_t)(sign | pick);
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits with bias 15, 10 fraction bits;
+ * exponent field 0 holds the subnormals f * 2^-24. Every value is exact in
+ * binary32. (Infinities and NaN are not inputs, reading R7.) */
+static float f16_bits_to_float(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double mag;
+    if (e == 0) mag = ldexp((double)f, -24);
+    else if (e == 31) mag = f ? NAN : INFINITY;
+    else mag = ldexp(1024.0 + f, e - 25);
+    return (float)(sign ? -mag : mag);
 }
 
 /* E4M3 (OCP): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits.
@@ -288,8 +315,8 @@ int bqo_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint16_t *x_loc
  * covers columns [32g, 32g + 32). A slice is addressed by offsetting the three
  * pointers; [ST] Compatibility asks for 128-column alignment, checked here on
  * cols only because the offset is the caller's pointer arithmetic. */
-int bqo_quant_mx(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
-                 uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s)
+static int quant_mx_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q,
+                         int64_t ld_q, uint8_t *s, int64_t ld_s, float (*widen)(uint16_t))
 {
     if (rows < 0 || cols < 0 || cols % 128) return -1;
     if (ld_x < cols || ld_q < cols || ld_s < cols / BQO_GROUP) return -1;
@@ -298,20 +325,36 @@ int bqo_quant_mx(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
             const uint16_t *xg = x + r * ld_x + g * BQO_GROUP;
             float amax = 0.0f;
             for (int i = 0; i < BQO_GROUP; i++) {
-                float a = fabsf(bf16_bits_to_float(xg[i]));
+                float a = fabsf(widen(xg[i]));
                 if (a > amax) amax = a;
             }
             uint8_t e = bqo_e8m0_scale(amax);
             s[r * ld_s + g] = e;
             for (int i = 0; i < BQO_GROUP; i++) {
                 /* reading R6: exact scaling by 2^(127-e) (in double, no rounding) */
-                double y = ldexp((double)bf16_bits_to_float(xg[i]), 127 - (int)e);
+                double y = ldexp((double)widen(xg[i]), 127 - (int)e);
                 q[r * ld_q + g * BQO_GROUP + i] = bqo_e4m3_encode(y);
             }
         }
     }
     return 0;
 }
+
+int bqo_quant_mx(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                 uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s)
+{
+    return quant_mx_rows(x, rows, cols, ld_x, q, ld_q, s, ld_s, bf16_bits_to_float);
+}
+
+/* The same for an FP16 input slice (reading R15). */
+int bqo_quant_mx_f16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ld_x,
+                     uint8_t *q, int64_t ld_q, uint8_t *s, int64_t ld_s)
+{
+    return quant_mx_rows(x, rows, cols, ld_x, q, ld_q, s, ld_s, f16_bits_to_float);
+}
+
+/* FP16 bits -> binary32 (exposed for the pins). */
+float bqo_f16_to_float(uint16_t h) { return f16_bits_to_float(h); }
 
 /* E4M3 + E8M0 -> BF16: out = BF16(decode(byte) * 2^(e-127)); the product is a
  * 4-significant-bit number >= 2^-136 and so exact, leaving one rounding. */
@@ -399,6 +442,99 @@ int bqo_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const uint16_t *x_
         quant_group_mx(v, q_out + g * BQO_GROUP, s_out + g);
     }
     if (out) bqo_dequant_mx(q_out, n, s_out, n / BQO_GROUP, n ? 1 : 0, n, out, n);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The i8 mode's BF16 reduce-scatter fused with the INT8 all-gather payload. */
+/* ------------------------------------------------------------------------ */
+
+/* Reading R13: for every element, acc = x_0 + x_1 + ... + x_{W-1} in binary32 in
+ * rank order, y = BF16(acc); each 128-value block of y is quantized like
+ * quant_i8; out (when not NULL) receives the materialization of the payload. */
+int bqo_reduce_quant_i8(const uint16_t *const *x_srcs, int W, int64_t n, int8_t *q, float *scales,
+                        uint16_t *out)
+{
+    if (n < 0 || n % BQO_BLOCK || W < 1) return -1;
+    float y[BQO_BLOCK];
+    for (int64_t b = 0; b < n / BQO_BLOCK; b++) {
+        for (int i = 0; i < BQO_BLOCK; i++) {
+            int64_t e = b * BQO_BLOCK + i;
+            float a = bf16_bits_to_float(x_srcs[0][e]);
+            for (int w = 1; w < W; w++) a = a + bf16_bits_to_float(x_srcs[w][e]);
+            y[i] = bf16_bits_to_float(bqo_bf16_round((double)a));
+        }
+        quant_block_i8(y, q + b * BQO_BLOCK, scales + b);
+    }
+    if (out) bqo_dequant_i8(q, scales, n, out);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Legacy E4M3 codec (reading R14): one E4M3 byte per value, one FP32 scale  */
+/* per 128-value block, the same 132-byte block as block INT8.               */
+/* ------------------------------------------------------------------------ */
+
+static void quant_block_e4m3(const float *v, uint8_t *q, float *scale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < BQO_BLOCK; i++) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    *scale = s;
+    for (int i = 0; i < BQO_BLOCK; i++) {
+        if (s == 0.0f) {
+            q[i] = 0;
+            continue;
+        }
+        float t = v[i] / s;   /* binary32 quotient, then the E4M3 grid */
+        q[i] = bqo_e4m3_encode((double)t);
+    }
+}
+
+int bqo_quant_e4m3(const uint16_t *x, int64_t n, uint8_t *q, float *scales)
+{
+    if (n < 0 || n % BQO_BLOCK) return -1;
+    float v[BQO_BLOCK];
+    for (int64_t b = 0; b < n / BQO_BLOCK; b++) {
+        for (int i = 0; i < BQO_BLOCK; i++) v[i] = bf16_bits_to_float(x[b * BQO_BLOCK + i]);
+        quant_block_e4m3(v, q + b * BQO_BLOCK, scales + b);
+    }
+    return 0;
+}
+
+/* out = BF16(fl(decode(code) * s)): decode is exact in binary32, the product is
+ * rounded to binary32, then to BF16 (two roundings, as for block INT8). */
+int bqo_dequant_e4m3(const uint8_t *q, const float *scales, int64_t n, uint16_t *out)
+{
+    if (n < 0 || n % BQO_BLOCK) return -1;
+    for (int64_t e = 0; e < n; e++) {
+        float d = (float)bqo_e4m3_decode(q[e]);
+        float p = d * scales[e / BQO_BLOCK];
+        out[e] = bqo_bf16_round((double)p);
+    }
+    return 0;
+}
+
+/* The E4M3 all-gather mode's BF16 reduce-scatter fused with its payload: R13 with
+ * the E4M3 codec in place of block INT8. */
+int bqo_reduce_quant_e4m3(const uint16_t *const *x_srcs, int W, int64_t n, uint8_t *q, float *scales,
+                          uint16_t *out)
+{
+    if (n < 0 || n % BQO_BLOCK || W < 1) return -1;
+    float y[BQO_BLOCK];
+    for (int64_t b = 0; b < n / BQO_BLOCK; b++) {
+        for (int i = 0; i < BQO_BLOCK; i++) {
+            int64_t e = b * BQO_BLOCK + i;
+            float a = bf16_bits_to_float(x_srcs[0][e]);
+            for (int w = 1; w < W; w++) a = a + bf16_bits_to_float(x_srcs[w][e]);
+            y[i] = bf16_bits_to_float(bqo_bf16_round((double)a));
+        }
+        quant_block_e4m3(y, q + b * BQO_BLOCK, scales + b);
+    }
+    if (out) bqo_dequant_e4m3(q, scales, n, out);
     return 0;
 }
 

@@ -204,3 +204,39 @@ def dequant_mx(code: int, e: int) -> int:
     """BF16 bits of decode(code) * 2^(e-127) (exact product, one rounding)."""
     v, _ = mx_element(code, e)
     return bf16_bits_signed(v, bool(code & 0x80))
+
+
+# ---- legacy E4M3 codec (reading R14) and FP16 inputs
+def quant_block_e4m3(vals):
+    """vals: 128 (exact binary32 value, is negative zero) pairs -> (codes, scale)."""
+    amax = max(abs(v) for v, _ in vals)
+    s = f32(amax / 448)
+    codes = []
+    for v, neg0 in vals:
+        if s == 0:
+            codes.append(0)
+            continue
+        t = f32(v / s)
+        c = e4m3_nearest(t)
+        if t == 0 and (neg0 or v < 0):
+            c = 0x80
+        codes.append(c)
+    return codes, s
+
+
+def dequant_e4m3(code: int, s: F) -> int:
+    """BF16 bits of fl(decode(code) * s), then BF16 (two roundings)."""
+    mag = dict(_E4M3)[code & 0x7F]
+    neg = bool(code & 0x80)
+    p = f32((-mag if neg else mag) * s)
+    return bf16_bits_signed(p, neg and s != 0)
+
+
+def f16_value(bits: int) -> F:
+    """Exact value of an IEEE binary16 bit pattern, from its definition."""
+    sign = -1 if bits & 0x8000 else 1
+    e = (bits >> 10) & 0x1F
+    f = bits & 0x3FF
+    if e == 0:
+        return sign * F(f) * F(2) ** -24
+    return sign * (1 + F(f, 1024)) * F(2) ** (e - 15)

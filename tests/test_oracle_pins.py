@@ -180,7 +180,7 @@ def test_half_step_error_bound():
 
 
 # ------------------------------------------------------------------ brute force (exact rationals)
-def _adversarial_blocks(rnd, nblk):
+def _adversarial_blocks(rnd, nblk, max_abs=3.0e38):
     special = [0.0, -0.0, 1.0, -1.0, 0.5, 1.5, 2.5, 127.0, 126.5, 2.0 ** -133, 2.0 ** -126, 3.0e38, -3.0e38]
     blocks = []
     for b in range(nblk):
@@ -195,7 +195,7 @@ def _adversarial_blocks(rnd, nblk):
             else:
                 vals.append(rnd.gauss(0, 1) * base)
         blocks.append(vals)
-    t = torch.tensor(blocks, dtype=torch.float32).clamp(-3.0e38, 3.0e38).to(torch.bfloat16)
+    t = torch.tensor(blocks, dtype=torch.float32).clamp(-max_abs, max_abs).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
@@ -589,6 +589,207 @@ def test_e4m3_encode_of_fp32_values_at_and_around_every_tie():
         want = exact.e4m3_nearest(F(float(y)))
         assert oracle.e4m3_encode(float(y)) == want, float(y)
         assert oracle.e4m3_encode(-float(y)) == (want | 0x80), float(y)
+
+
+# ------------------------------------------------------------------ legacy E4M3 codec
+def _parse_e4m3_golden():
+    cases, cur = [], None
+    for line in open(os.path.join(GOLDEN, "e4m3_blocks.txt")):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        key, _, val = line.partition(":")
+        val = val.split()
+        if key == "case":
+            cur = {"name": val[0]}
+            cases.append(cur)
+        else:
+            cur[key] = val
+    return cases
+
+
+@pytest.mark.parametrize("case", _parse_e4m3_golden(), ids=lambda c: c["name"])
+def test_e4m3_golden_blocks(case):
+    xs = [float(v) for v in case["x"]]
+    block = np.zeros(128, np.uint16)
+    block[: len(xs)] = _bf16_bits_of(xs)
+    assert np.array_equal(_bits_to_f32(block[: len(xs)]), np.array(xs, np.float32))
+    q, s = oracle.quant_e4m3(block)
+    assert int(s.view(np.uint32)[0]) == int(case["scale_bits"][0], 16)
+    assert [int(v) for v in q[: len(xs)]] == [int(c, 16) for c in case["codes"]]
+    assert np.all(q[len(xs):] == 0)
+    out = oracle.dequant_e4m3(q, s)
+    assert [int(h, 16) for h in case["deq"]] == list(out[: len(xs)].astype(int))
+
+
+def test_e4m3_amax_maps_to_448_for_every_bf16_amax():
+    # Reading R14 with a BF16 amax a: s = fl(a / 448) (checked against numpy's binary32
+    # division) and the element holding the amax encodes to +-448 (0x7e / 0xfe) for
+    # every positive finite BF16 amax: fl(a / s) lies within 0.34% of 448 even where s
+    # is a binary32 subnormal, and 448 is the nearest (or saturated) E4M3 value.
+    a_bits = np.arange(1, 0x7F80, dtype=np.uint16)
+    blocks = np.zeros((a_bits.size, 128), np.uint16)
+    blocks[:, 0] = a_bits
+    blocks[:, 77] = a_bits | 0x8000
+    blocks[:, 5] = 0x8000
+    q, s = oracle.quant_e4m3(blocks.reshape(-1))
+    q = q.reshape(-1, 128)
+    a = _bits_to_f32(a_bits)
+    assert np.array_equal(s, (a / np.float32(448.0)).astype(np.float32))
+    assert np.all(q[:, 0] == 0x7E) and np.all(q[:, 77] == 0xFE)
+    assert np.all(q[:, 5] == 0x80)  # -0 in a non-zero block keeps its sign
+    assert np.all(q[:, [1, 2, 3, 4, 6, 100]] == 0)
+
+
+def test_e4m3_codec_brute_force_exact():
+    rnd = random.Random(21)
+    x = _adversarial_blocks(rnd, 16).reshape(-1)
+    q, s = oracle.quant_e4m3(x)
+    out = oracle.dequant_e4m3(q, s)
+    for b in range(16):
+        vals = [(exact.bits_to_value(int(v)), int(v) == 0x8000) for v in x[128 * b:128 * b + 128]]
+        codes, sc = exact.quant_block_e4m3(vals)
+        assert F(float(s[b])) == sc, b
+        assert [int(c) for c in q[128 * b:128 * b + 128]] == codes, b
+        assert [int(o) for o in out[128 * b:128 * b + 128]] == [exact.dequant_e4m3(c, sc) for c in codes], b
+
+
+def test_e4m3_dequant_rounds_twice():
+    # As for block INT8 (reading R3 applied by R14): decode(code) * s is rounded to
+    # binary32, then to BF16. Search binary32 scales next to m / d for BF16 midpoints m
+    # and E4M3 values d with more than one significant bit, where the two roundings
+    # differ from one rounding of the exact product, and check the oracle rounds twice.
+    found = 0
+    vals = dict(exact.e4m3_values())
+    for m in (1 + F(1, 256), 1 + F(3, 256), F(3, 2) + F(1, 128), 100 + F(1, 4)):
+        for code in (0x39, 0x3B, 0x3D, 0x3F, 0x43, 0x47, 0x4D, 0x55):
+            d = vals[code]
+            centre = np.float32(float(m / d))
+            cands = [centre]
+            lo = hi = centre
+            for _ in range(3):
+                lo = np.nextafter(lo, np.float32(0), dtype=np.float32)
+                hi = np.nextafter(hi, np.float32(np.inf), dtype=np.float32)
+                cands += [lo, hi]
+            for sc in cands:
+                exact_prod = d * F(float(sc))
+                once = exact.bf16_bits(exact.bf16(exact_prod))
+                twice = exact.bf16_bits(exact.bf16(exact.f32(exact_prod)))
+                if once != twice:
+                    qq = np.zeros(128, np.uint8)
+                    qq[0] = code
+                    assert int(oracle.dequant_e4m3(qq, np.array([sc], np.float32))[0]) == twice
+                    found += 1
+    assert found >= 3
+
+
+# ------------------------------------------------------------------ BF16 reduce + quantize
+def test_reduce_quant_follows_rank_order_then_bf16_exact():
+    # Reading R13: binary32 sum in rank order, one rounding to BF16, then the codec.
+    rnd = random.Random(22)
+    W = 4
+    xs = [_adversarial_blocks(rnd, 6, max_abs=1.0e37).reshape(-1) for _ in range(W)]  # sums stay finite
+    # block 0: big, tiny, -big, tiny (the order is visible); block 1: negative zeros
+    xs[0][:128], xs[2][:128] = 0x4B80, 0xCB80  # +-2^24
+    xs[1][:128], xs[3][:128] = 0x3F80, 0x3F80  # 1
+    for w in range(W):
+        xs[w][128:256] = 0x8000
+    xs[1][130] = 0x0000
+    qi, si, oi = oracle.reduce_quant_i8(xs, materialize=True)
+    qe, se, oe = oracle.reduce_quant_e4m3(xs, materialize=True)
+    for b in range(6):
+        y = []
+        for i in range(128):
+            e = 128 * b + i
+            a = (exact.bits_to_value(int(xs[0][e])), int(xs[0][e]) == 0x8000)
+            for w in range(1, W):
+                a = exact.f32_add_signed(a, (exact.bits_to_value(int(xs[w][e])), int(xs[w][e]) == 0x8000))
+            y.append((exact.bf16(a[0]), a[1]))
+        q_ref, s_ref = exact.quant_block_i8([v for v, _ in y])
+        assert F(float(si[b])) == s_ref and list(qi[128 * b:128 * b + 128]) == q_ref, b
+        c_ref, se_ref = exact.quant_block_e4m3(y)
+        assert F(float(se[b])) == se_ref and [int(c) for c in qe[128 * b:128 * b + 128]] == c_ref, b
+    # the order matters in block 0: ((2^24 + 1) - 2^24) + 1 = 1 in binary32 (2^24 + 1
+    # rounds to 2^24), while (2^24 - 2^24) + (1 + 1) = 2
+    d = [exact.bits_to_value(int(xs[w][0])) for w in range(W)]
+    in_order = exact.f32(exact.f32(exact.f32(d[0] + d[1]) + d[2]) + d[3])
+    regrouped = exact.f32(exact.f32(d[0] + d[2]) + exact.f32(d[1] + d[3]))
+    assert in_order != regrouped
+    # canonical forwarding
+    assert np.array_equal(oi, oracle.dequant_i8(qi, si))
+    assert np.array_equal(oe, oracle.dequant_e4m3(qe, se))
+
+
+def test_reduce_quant_of_one_source_is_quantize():
+    rnd = random.Random(23)
+    x = _adversarial_blocks(rnd, 12).reshape(-1)
+    qi, si, _ = oracle.reduce_quant_i8([x])
+    q0, s0 = oracle.quant_i8(x)
+    assert np.array_equal(qi, q0) and np.array_equal(si, s0)
+    qe, se, _ = oracle.reduce_quant_e4m3([x])
+    q1, s1 = oracle.quant_e4m3(x)
+    assert np.array_equal(qe, q1) and np.array_equal(se, s1)
+
+
+# ------------------------------------------------------------------ FP16 slices for MX
+def test_f16_widening_exhaustive_vs_numpy():
+    bits = np.arange(0, 0x10000, dtype=np.uint32)
+    finite = ((bits >> 10) & 0x1F) != 0x1F
+    bits = bits[finite].astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_to_float(int(b)) for b in bits], np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_mx_f16_scale_exhaustive_over_fp16_amax():
+    # every positive finite FP16 amax against the frexp closed form of fl(a / 448)
+    a_bits = np.arange(1, 0x7C00, dtype=np.uint16)
+    a = a_bits.view(np.float16).astype(np.float32)
+    v = (a / np.float32(448.0)).astype(np.float32)
+    m, k = np.frexp(v.astype(np.float64))
+    expect = np.clip(np.where(m == 0.5, k - 1, k) + 127, 0, 254)
+    ng = ((a_bits.size + 3) // 4) * 4
+    groups = np.zeros((ng, 32), np.uint16)
+    groups[: a_bits.size, 0] = a_bits
+    groups[: a_bits.size, 9] = a_bits | 0x8000
+    q, s = oracle.quant_mx(groups.reshape(-1, 128), fmt="f16")
+    got = s.reshape(-1)[: a_bits.size]
+    assert np.array_equal(got, expect.astype(np.uint8))
+    codes = q.reshape(-1, 32)[: a_bits.size]
+    y = a.astype(np.float64) * np.exp2(127.0 - got.astype(np.float64))
+    assert np.all(y <= 448.0) and np.all(y > 224.0)  # FP16's range never reaches byte 0
+    assert np.all((codes[:, 9] & 0x80) == 0x80)
+
+
+def test_mx_f16_brute_force_exact():
+    rng = np.random.default_rng(24)
+    vals = (rng.standard_normal((8, 128)) * 10.0 ** rng.uniform(-6, 4, (8, 1))).astype(np.float16)
+    vals[0, :8] = np.array([65504, -65504, 6e-8, -6e-8, 0.0, -0.0, 1.0, 0.5], np.float16)
+    vals[1, :32] = np.float16(2.0 ** -24) * np.arange(32)
+    x = vals.view(np.uint16)
+    q, s = oracle.quant_mx(x, fmt="f16")
+    for r in range(8):
+        for g in range(4):
+            vs = [exact.f16_value(int(b)) for b in x[r, 32 * g:32 * g + 32]]
+            amax = max(abs(v) for v in vs)
+            e = 127 if amax == 0 else exact.e8m0_up(exact.f32(amax / 448))
+            assert s[r, g] == e
+            for i, v in enumerate(vs):
+                c = exact.e4m3_nearest(v * F(2) ** (127 - e))
+                if v == 0 and x[r, 32 * g + i] & 0x8000:
+                    c = 0x80
+                assert q[r, 32 * g + i] == c
+
+
+def test_mx_f16_staged_slices_equal_concatenated():
+    rng = np.random.default_rng(25)
+    slices = [(rng.standard_normal((16, 256)) * 30).astype(np.float16).view(np.uint16) for _ in range(3)]
+    q_buf = np.zeros((16, 768), np.uint8)
+    s_buf = np.zeros((16, 24), np.uint8)
+    for i, sl in enumerate(slices):
+        oracle.quant_mx_into(sl, q_buf, s_buf, 256 * i, fmt="f16")
+    q, s = oracle.quant_mx(np.concatenate(slices, axis=1), fmt="f16")
+    assert np.array_equal(q_buf, q) and np.array_equal(s_buf, s)
 
 
 # ------------------------------------------------------------------ staged == concatenated
