@@ -64,6 +64,11 @@ def kernel_bytes(name: str, n: int) -> int:
         "dequant_mx": w + BF16,
         "dequant_accum_mx": W_SRC * w + w,
         "ring_hop_mx": w + BF16 + w,
+        "reduce_quant_i8": W_SRC * BF16 + w,
+        "reduce_quant_e4m3": W_SRC * BF16 + w,
+        "quant_e4m3": BF16 + w,
+        "dequant_e4m3": w + BF16,
+        "quant_mx_f16": BF16 + w,
     }[name]
     return int(round(per * n))
 
@@ -332,23 +337,48 @@ def cpu_inputs(rows: int, slice_rows: int):
 
 # ---------------------------------------------------------------- widened rows
 def time_next_rows(pipe, args, peak):
-    """Per-launch duration of dequant_accum_mx (W=4) and ring_hop_mx over the prefill
-    buffers as flat MX wires: CUDA events around `reps` back-to-back launches of each
-    kernel on the launching stream, after 3 warm-up launches. Every launch reads and
-    writes more than the 129 MB L2 holds, so launches do not hit in L2."""
+    """Per-launch duration of the kernels beyond the step, on the prefill buffers:
+    dequant_accum_mx (W=4) and ring_hop_mx on flat MX wires quantized from them,
+    reduce_quant_i8 / reduce_quant_e4m3 (W=4: the all-gather modes' fused reduce),
+    quant_e4m3 / dequant_e4m3 (legacy codec), and quant_mx on FP16 slices of the staged
+    workload (rotating over six slices). CUDA events around `next_reps` back-to-back
+    launches of each kernel on the launching stream, after 3 warm-up launches; every
+    launch (or, for the slices, every six consecutive launches) moves more than the
+    129 MB L2 holds."""
+    from block_quantized_wire_gb300 import inputs
     c = pipe.codec
     n = pipe.n
-    wires = [c.empty_wire_mx(n, pipe.xs[0].device) for _ in range(W_SRC + 2)]
+    dev = pipe.xs[0].device
+    xs = [x.view(-1) for x in pipe.xs]
+    wires = [c.empty_wire_mx(n, dev) for _ in range(W_SRC + 2)]
     for w in range(W_SRC):
-        c.quant_mx_flat(pipe.xs[w].view(-1), wires[w][1], wires[w][2])
+        c.quant_mx_flat(xs[w], wires[w][1], wires[w][2])
     acc, hop = wires[W_SRC], wires[W_SRC + 1]
+    ew = c.empty_wire_e4m3(n, dev)
+    iw = c.empty_wire_i8(n, dev)
+    c.quant_e4m3(xs[0], ew[1], ew[2])
+    f16 = inputs.mx_slices_4096(device=dev, rows=pipe.slice_rows, dtype=torch.float16)
+    ns = f16[0].numel()
+    turn = [0]
+
+    def quant_f16():
+        i = turn[0] % len(f16)
+        turn[0] += 1
+        c0 = i * HIDDEN
+        c.quant_mx(f16[i], pipe.mx_q[:, c0:c0 + HIDDEN], pipe.mx_s[:, c0 // 32:(c0 + HIDDEN) // 32])
+
     runs = {
-        "dequant_accum_mx": lambda: c.dequant_accum_mx([wires[w][1] for w in range(W_SRC)],
-                                                       [wires[w][2] for w in range(W_SRC)], acc[1], acc[2], None),
-        "ring_hop_mx": lambda: c.ring_hop_mx(wires[0][1], wires[0][2], pipe.xs[1].view(-1), hop[1], hop[2], None),
+        "dequant_accum_mx": (lambda: c.dequant_accum_mx([wires[w][1] for w in range(W_SRC)],
+                                                        [wires[w][2] for w in range(W_SRC)], acc[1], acc[2], None), n),
+        "ring_hop_mx": (lambda: c.ring_hop_mx(wires[0][1], wires[0][2], xs[1], hop[1], hop[2], None), n),
+        "reduce_quant_i8": (lambda: c.reduce_quant_i8(xs, iw[1], iw[2], None), n),
+        "reduce_quant_e4m3": (lambda: c.reduce_quant_e4m3(xs, ew[1], ew[2], None), n),
+        "quant_e4m3": (lambda: c.quant_e4m3(xs[2], ew[1], ew[2]), n),
+        "dequant_e4m3": (lambda: c.dequant_e4m3(ew[1], ew[2], pipe.out.view(-1)), n),
+        "quant_mx_f16": (quant_f16, ns),
     }
     out = {}
-    for name, fn in runs.items():
+    for name, (fn, nv) in runs.items():
         for _ in range(3):
             fn()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -359,11 +389,11 @@ def time_next_rows(pipe, args, peak):
         e1.record()
         torch.cuda.synchronize()
         avg_ms = e0.elapsed_time(e1) / args.next_reps
-        nbytes = kernel_bytes(name, n)
+        nbytes = kernel_bytes(name, nv)
         gbs = nbytes / (avg_ms * 1e-3) / 1e9
         out[name] = {"launches": args.next_reps, "avg_us": round(avg_ms * 1e3, 2), "bytes_per_launch": nbytes,
                      "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
-    del wires
+    del wires, ew, iw, f16
     return out
 
 
@@ -544,7 +574,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip timing the MX wire reductions")
-    ap.add_argument("--next-reps", type=int, default=20)
+    ap.add_argument("--next-reps", type=int, default=24)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-slice-rows", type=int, default=256)
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of CPU work for --impl reference")

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libbq.so")
 OBJDIR = os.path.join(PKG, "_build")
 
-SOURCES = ["bq_api.cu", "bq_i8.cu", "bq_mx.cu", "bq_mx_wire.cu"]
+SOURCES = ["bq_api.cu", "bq_i8.cu", "bq_mx.cu", "bq_mx_wire.cu", "bq_e4m3.cu"]
 HEADERS = ["bq_device.cuh", "bq_launch.h", "bq_chunks.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

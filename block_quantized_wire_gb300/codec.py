@@ -143,17 +143,20 @@ def ring_hop_i8(q_in: torch.Tensor, s_in: torch.Tensor, x_local: torch.Tensor, q
 
 # ---------------------------------------------------------------- MXFP8
 def quant_mx(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
-    """BF16 x [rows, cols] -> E4M3 q [rows, cols] + E8M0 s [rows, cols/32].
+    """BF16 or FP16 x [rows, cols] -> E4M3 q [rows, cols] + E8M0 s [rows, cols/32].
 
     Any of the three may be a column slice of a wider row-major buffer, e.g.
     ``q_buf[:, c0:c0+cols]`` and ``s_buf[:, c0//32:(c0+cols)//32]`` with c0 % 128 == 0.
+    The input's dtype selects bq_quant_mx (BF16) or bq_quant_mx_f16 (FP16).
     """
-    xp, rows, cols, ld_x = _rows(x, torch.bfloat16, "x")
+    f16 = x.dtype == torch.float16
+    xp, rows, cols, ld_x = _rows(x, torch.float16 if f16 else torch.bfloat16, "x")
     qp, qr, qc, ld_q = _rows(q, torch.uint8, "q")
     sp, sr, sc, ld_s = _rows(s, torch.uint8, "s")
     if (qr, qc) != (rows, cols) or (sr, sc) != (rows, cols // GROUP_MX):
         raise ValueError("quant_mx: output shapes do not match x")
-    check("bq_quant_mx", load().bq_quant_mx(xp, rows, cols, ld_x, qp, ld_q, sp, ld_s, _stream(stream)))
+    name = "bq_quant_mx_f16" if f16 else "bq_quant_mx"
+    check(name, getattr(load(), name)(xp, rows, cols, ld_x, qp, ld_q, sp, ld_s, _stream(stream)))
 
 
 def dequant_mx(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor, stream=None) -> None:
@@ -211,6 +214,62 @@ def ring_hop_mx(q_in: torch.Tensor, s_in: torch.Tensor, x_local: torch.Tensor, q
         _flat(q_in, torch.uint8, "q_in"), _flat(s_in, torch.uint8, "s_in"), _flat(x_local, torch.bfloat16, "x_local"),
         n, _flat(q_out, torch.uint8, "q_out"), _flat(s_out, torch.uint8, "s_out"),
         _flat(out, torch.bfloat16, "out") if out is not None else None, _stream(stream)))
+
+
+# ---------------------------------------------------------------- reduce + quantize, legacy E4M3
+def _reduce_quant(name, x_srcs, q, scales, out, stream, qtype):
+    W = len(x_srcs)
+    n = q.numel()
+    for x in x_srcs:
+        if x.numel() != n:
+            raise ValueError(f"{name}: a source's size differs from the payload's")
+    if scales.numel() * BLOCK_I8 != n or (out is not None and out.numel() != n):
+        raise ValueError(f"{name}: output sizes do not match")
+    xp = (ctypes.c_void_p * max(W, 1))(*[_flat(x, torch.bfloat16, "x_srcs[]") for x in x_srcs])
+    check(name, getattr(load(), name)(
+        ctypes.cast(xp, ctypes.c_void_p), W, n, _flat(q, qtype, "q"), _flat(scales, torch.float32, "scales"),
+        _flat(out, torch.bfloat16, "out") if out is not None else None, _stream(stream)))
+
+
+def reduce_quant_i8(x_srcs: Sequence[torch.Tensor], q: torch.Tensor, scales: torch.Tensor,
+                    out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The i8 mode's BF16 reduce fused with quant_i8: W BF16 shards summed in list (rank)
+    order in FP32, rounded once to BF16, quantized into q/scales; optionally the
+    owner's materialization into out."""
+    _reduce_quant("bq_reduce_quant_i8", x_srcs, q, scales, out, stream, torch.int8)
+
+
+def empty_wire_e4m3(n: int, device="cuda"):
+    """One contiguous n-value legacy E4M3 wire: (buffer, codes uint8 [n], scales float32 [n/128])."""
+    nbytes = wire_bytes(n)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return buf, buf[:n], buf[n:].view(torch.float32)
+
+
+def quant_e4m3(x: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """BF16 x [n] -> legacy E4M3 codes q [n] (uint8) + FP32 scales [n/128]."""
+    n = x.numel()
+    if q.numel() != n or scales.numel() * BLOCK_I8 != n:
+        raise ValueError("quant_e4m3: output sizes do not match x")
+    check("bq_quant_e4m3", load().bq_quant_e4m3(
+        _flat(x, torch.bfloat16, "x"), n, _flat(q, torch.uint8, "q"), _flat(scales, torch.float32, "scales"),
+        _stream(stream)))
+
+
+def dequant_e4m3(q: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Legacy E4M3 codes q [n] + scales [n/128] -> BF16 out [n]."""
+    n = q.numel()
+    if out.numel() != n or scales.numel() * BLOCK_I8 != n:
+        raise ValueError("dequant_e4m3: sizes do not match")
+    check("bq_dequant_e4m3", load().bq_dequant_e4m3(
+        _flat(q, torch.uint8, "q"), _flat(scales, torch.float32, "scales"), n, _flat(out, torch.bfloat16, "out"),
+        _stream(stream)))
+
+
+def reduce_quant_e4m3(x_srcs: Sequence[torch.Tensor], q: torch.Tensor, scales: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """reduce_quant_i8 with the legacy E4M3 codec (the E4M3 all-gather mode)."""
+    _reduce_quant("bq_reduce_quant_e4m3", x_srcs, q, scales, out, stream, torch.uint8)
 
 
 # ---------------------------------------------------------------- bounded waits

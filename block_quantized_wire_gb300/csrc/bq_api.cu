@@ -274,6 +274,94 @@ bq_status bq_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const void *x
                                              stream));
 }
 
+bq_status bq_quant_mx_f16(const void *x_f16, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q_e4m3, int64_t ld_q,
+                          uint8_t *s_e8m0, int64_t ld_s, cudaStream_t stream)
+{
+    if (rows < 0 || cols < 0 || cols % 128) return BQ_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return BQ_OK;
+    if (ld_x < cols || ld_q < cols || ld_s < cols / BQ_GROUP_MX) return BQ_ERR_SHAPE;
+    if (!x_f16 || !q_e4m3 || !s_e8m0) return BQ_ERR_NULL;
+    if (!aligned(x_f16, 16) || ld_x % 8 || !aligned(q_e4m3, 16) || ld_q % 16 || !aligned(s_e8m0, 4) || ld_s % 4)
+        return BQ_ERR_ALIGN;
+    const Range ins[] = {span2d(x_f16, rows, 2 * cols, 2 * ld_x)};
+    const Range outs[] = {span2d(q_e4m3, rows, cols, ld_q), span2d(s_e8m0, rows, cols / BQ_GROUP_MX, ld_s)};
+    if (any_alias(outs, 2, ins, 1)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_quant_mx_f16(static_cast<const uint16_t *>(x_f16), ld_x, rows, cols, q_e4m3, ld_q,
+                                              s_e8m0, ld_s, stream));
+}
+
+namespace {
+// Shared checks of the reduce + quantize calls: W BF16 sources -> payload [n] (1 byte
+// per value, 16-byte aligned), FP32 scales [n/128] (4-byte aligned), optional BF16.
+bq_status check_reduce(const void *const *x_srcs, int W, int64_t n, const void *q, const void *scales,
+                       const void *out_bf16, bqk::Bf16List *src)
+{
+    if (W < 1 || W > BQ_MAX_W) return BQ_ERR_SHAPE;
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!x_srcs || !q || !scales) return BQ_ERR_NULL;
+    Range ins[BQ_MAX_W];
+    for (int w = 0; w < W; w++) {
+        if (!x_srcs[w]) return BQ_ERR_NULL;
+        if (!aligned(x_srcs[w], 16)) return BQ_ERR_ALIGN;
+        src->x[w] = static_cast<const uint16_t *>(x_srcs[w]);
+        ins[w] = span(x_srcs[w], 2 * n);
+    }
+    if (!aligned(q, 16) || !aligned(scales, 4) || (out_bf16 && !aligned(out_bf16, 16))) return BQ_ERR_ALIGN;
+    Range outs[3] = {span(q, n), span(scales, 4 * (n / BQ_BLOCK_I8)), {}};
+    int n_out = 2;
+    if (out_bf16) outs[n_out++] = span(out_bf16, 2 * n);
+    if (any_alias(outs, n_out, ins, W)) return BQ_ERR_ALIAS;
+    return BQ_OK;
+}
+}  // namespace
+
+bq_status bq_reduce_quant_i8(const void *const *x_srcs, int W, int64_t n, int8_t *q, float *scales, void *out_bf16,
+                             cudaStream_t stream)
+{
+    bqk::Bf16List src = {};
+    if (bq_status e = check_reduce(x_srcs, W, n, q, scales, out_bf16, &src)) return e;
+    if (n == 0) return BQ_OK;
+    return from_cuda(bqk::launch_reduce_quant_i8(src, W, n / BQ_BLOCK_I8, q, scales,
+                                                 static_cast<uint16_t *>(out_bf16), stream));
+}
+
+bq_status bq_quant_e4m3(const void *x_bf16, int64_t n, uint8_t *q, float *scales, cudaStream_t stream)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!x_bf16 || !q || !scales) return BQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(q, 16) || !aligned(scales, 4)) return BQ_ERR_ALIGN;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    const Range ins[] = {span(x_bf16, 2 * n)};
+    const Range outs[] = {span(q, n), span(scales, 4 * nblk)};
+    if (any_alias(outs, 2, ins, 1)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_quant_e4m3(static_cast<const uint16_t *>(x_bf16), nblk, q, scales, stream));
+}
+
+bq_status bq_dequant_e4m3(const uint8_t *q, const float *scales, int64_t n, void *out_bf16, cudaStream_t stream)
+{
+    if (n < 0 || n % BQ_BLOCK_I8) return BQ_ERR_SHAPE;
+    if (n == 0) return BQ_OK;
+    if (!q || !scales || !out_bf16) return BQ_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(scales, 4) || !aligned(out_bf16, 16)) return BQ_ERR_ALIGN;
+    const int64_t nblk = n / BQ_BLOCK_I8;
+    const Range ins[] = {span(q, n), span(scales, 4 * nblk)};
+    const Range outs[] = {span(out_bf16, 2 * n)};
+    if (any_alias(outs, 1, ins, 2)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_dequant_e4m3(q, scales, nblk, static_cast<uint16_t *>(out_bf16), stream));
+}
+
+bq_status bq_reduce_quant_e4m3(const void *const *x_srcs, int W, int64_t n, uint8_t *q, float *scales,
+                               void *out_bf16, cudaStream_t stream)
+{
+    bqk::Bf16List src = {};
+    if (bq_status e = check_reduce(x_srcs, W, n, q, scales, out_bf16, &src)) return e;
+    if (n == 0) return BQ_OK;
+    return from_cuda(bqk::launch_reduce_quant_e4m3(src, W, n / BQ_BLOCK_I8, q, scales,
+                                                   static_cast<uint16_t *>(out_bf16), stream));
+}
+
 bq_status bq_take_wait_timeouts(int64_t *count)
 {
     if (!count) return BQ_ERR_NULL;

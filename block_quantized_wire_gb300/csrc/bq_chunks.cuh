@@ -17,7 +17,10 @@
 //     template <int SEGS, bool kTail, bool kOut>
 //     static void requant(const float2 (&v)[SEGS][4], int64_t e0, int64_t b0,
 //                         int64_t nblk, int lane, Q *q, S *s, uint16_t *out);
+//     // BF16 materialization of a lane's 8 payload elements
+//     static uint4 dequant8(uint2 payload, uint32_t word, int lane);
 //   };
+// (a policy defines only what the ops it is used with call).
 //
 // The reductions are the all-to-all accumulate (sources decoded and added left to
 // right in source order in binary32, then requantized) and the ring hop (incoming
@@ -145,6 +148,174 @@ __device__ __forceinline__ void run_staged(const Op &op, int64_t nblk, int chunk
         op.template compute<true>(t, c);
     }
 }
+
+// Lane-held amax of each segment -> lane 2j+h holds block (2j+h)'s amax.
+template <int SEGS>
+__device__ __forceinline__ float gather_amax(const float (&m)[SEGS], int lane)
+{
+    float mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < SEGS; j++) {
+        const float g = __shfl_sync(kFull, m[j], (lane & 1) << 4);
+        if ((lane >> 1) == j) mine = g;
+    }
+    return mine;
+}
+
+// ---------------------------------------------------------------- quantize
+template <class Codec, int SEGS>
+struct QuantOp {
+    const uint16_t *__restrict__ x;
+    typename Codec::Q *__restrict__ q;
+    typename Codec::S *__restrict__ s;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint4 x[SEGS];
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+#pragma unroll
+        for (int j = 0; j < SEGS; j++)
+            in.x[j] = (!kTail || b0 + 2 * j + (lane >> 4) < nblk) ? ld_stream_v4(x + e0 + 256 * j)
+                                                                  : make_uint4(0, 0, 0, 0);
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float2 v[SEGS][4];
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
+        Codec::template requant<SEGS, kTail, false>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s,
+                                                    nullptr);
+    }
+    static constexpr uint32_t kStageBytes = 512u * SEGS;  // the chunk's BF16 values
+    static_assert(kStageBytes % 16 == 0, "bulk copies move whole 16-byte units");
+    __device__ __forceinline__ void issue(int64_t c, uint32_t stage, uint32_t bar) const
+    {
+        mbar_expect_tx(bar, kStageBytes);
+        bulk_load(stage, x + c * (256 * SEGS), kStageBytes, bar);
+    }
+    __device__ __forceinline__ void load_staged(In &in, const unsigned char *stage) const
+    {
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) in.x[j] = *reinterpret_cast<const uint4 *>(stage + 512 * j + 16 * lane);
+    }
+};
+
+// ---------------------------------------------------------------- materialize
+template <class Codec, int SEGS>
+struct DequantOp {
+    const typename Codec::Q *__restrict__ q;
+    const typename Codec::S *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint2 q[SEGS];
+        uint32_t sc;
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+#pragma unroll
+        for (int j = 0; j < SEGS; j++)
+            in.q[j] = (!kTail || b0 + 2 * j + (lane >> 4) < nblk) ? ld_stream_v2(q + e0 + 256 * j) : make_uint2(0, 0);
+        in.sc = (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) ? ld_stream_u32(s + b0 + lane) : 0u;
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+        const int half = lane >> 4;
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            const uint32_t wj = __shfl_sync(kFull, in.sc, 2 * j + half);
+            if (!kTail || b0 + 2 * j + half < nblk) st_v4(out + e0 + 256 * j, Codec::dequant8(in.q[j], wj, lane));
+        }
+    }
+};
+
+// ---------------------------------------------------------------- reduce + quantize
+// The all-gather modes' BF16 reduce-scatter fused with quantization of its result: the
+// W ranks' BF16 shards are added left to right in rank order in binary32, the sum is
+// rounded once to BF16 (the reduce-scatter's result) and widened back exactly, and the
+// codec quantizes it. The first W sources are loaded together; further sources in
+// groups of W.
+template <int SEGS, int W>
+struct Bf16Regs {
+    uint4 x[W][SEGS];
+};
+
+template <int SEGS, int W, bool kTail>
+__device__ __forceinline__ void load_bf16_sources(Bf16Regs<SEGS, W> &r, const Bf16List &src, int g, int nsrc,
+                                                  int64_t c, int64_t nblk, int lane)
+{
+    const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+#pragma unroll
+    for (int i = 0; i < W; i++) {
+        const bool src_ok = g + i < nsrc;
+        const uint16_t *xw = src.x[src_ok ? g + i : g];
+#pragma unroll
+        for (int j = 0; j < SEGS; j++)
+            r.x[i][j] = (src_ok && (!kTail || b0 + 2 * j + (lane >> 4) < nblk)) ? ld_stream_v4(xw + e0 + 256 * j)
+                                                                                 : make_uint4(0, 0, 0, 0);
+    }
+}
+
+template <int SEGS, int W, bool kFirst>
+__device__ __forceinline__ void add_bf16_sources(const Bf16Regs<SEGS, W> &r, int g, int nsrc, float2 (&acc)[SEGS][4])
+{
+#pragma unroll
+    for (int i = 0; i < W; i++) {
+        if (g + i >= nsrc) break;
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            float2 v[4];
+            bf16x8_to_f32(r.x[i][j], v);
+#pragma unroll
+            for (int e = 0; e < 4; e++) acc[j][e] = (kFirst && i == 0) ? v[e] : add2(acc[j][e], v[e]);
+        }
+    }
+}
+
+template <class Codec, int SEGS, int W, bool kOut>
+struct ReduceQuantOp {
+    const Bf16List &src;  // the kernel's __grid_constant__ parameter, read in place
+    int nsrc;
+    typename Codec::Q *__restrict__ q;
+    typename Codec::S *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    using In = Bf16Regs<SEGS, W>;
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        load_bf16_sources<SEGS, W, kTail>(in, src, 0, nsrc, c, nblk, lane);
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float2 acc[SEGS][4];
+        add_bf16_sources<SEGS, W, true>(in, 0, nsrc, acc);
+        for (int g = W; g < nsrc; g += W) {
+            In more;
+            load_bf16_sources<SEGS, W, kTail>(more, src, g, nsrc, c, nblk, lane);
+            add_bf16_sources<SEGS, W, false>(more, g, nsrc, acc);
+        }
+#pragma unroll
+        for (int j = 0; j < SEGS; j++) {
+            const uint4 rounded = f32x8_to_bf16x8(acc[j]);  // the reduce-scatter's BF16 result
+            bf16x8_to_f32(rounded, acc[j]);
+        }
+        Codec::template requant<SEGS, kTail, kOut>(acc, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q,
+                                                   s, out);
+    }
+};
 
 // ---------------------------------------------------------------- accumulate
 // Sources are summed in source order 0..nsrc-1. The first W sources of a chunk are

@@ -217,6 +217,17 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float2 v)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Eight FP16 values (one 16-byte load) -> binary32, exact.
+__device__ __forceinline__ void f16x8_to_f32(const uint4 w, float2 (&v)[4])
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const __half2 h = *reinterpret_cast<const __half2 *>(&u[i]);
+        v[i] = __half22float2(h);
+    }
+}
+
 __device__ __forceinline__ uint4 f32x8_to_bf16x8(const float2 (&v)[4])
 {
     return make_uint4(f32x2_to_bf16x2(v[0]), f32x2_to_bf16x2(v[1]), f32x2_to_bf16x2(v[2]), f32x2_to_bf16x2(v[3]));
@@ -393,7 +404,8 @@ __device__ __forceinline__ uint2 f32x8_to_e4m3x8(const float2 (&y)[4])
     return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
-// Eight E4M3 codes -> their exact binary32 values, each times p = 2^k (exact).
+// Eight E4M3 codes -> binary32 fl(decode(code) * p); the decode is exact, and so is
+// the product when p is a power of two.
 __device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float p, float2 (&v)[4])
 {
     const float2 p2 = splat(p);
@@ -408,6 +420,62 @@ __device__ __forceinline__ void e4m3x8_to_f32(uint2 w, float p, float2 (&v)[4])
             v[2 * j + i] = mul2(__half22float2(hh), p2);
         }
     }
+}
+
+// ---------------------------------------------------------------- legacy E4M3 codec
+// One FP32 scale s = fl(amax / 448) per 128-value block; code = E4M3 (nearest even,
+// saturating, sign of zero kept) of fl(x / s). The quotient uses the same Markstein
+// form as block INT8. Its remainder is exact when ulp(q) * ulp(s) >= 2^-149, i.e. when
+// the exponents of q and s sum to at least -103. With s >= 2^-90 that holds for every
+// quotient >= 2^-13, and smaller quotients round to E4M3 zero whatever their last bits.
+// Blocks with a smaller nonzero scale divide per element.
+constexpr float kE4m3QuotientMinScale = 8.07793567e-28f;  // 2^-90
+
+__device__ __forceinline__ I8Scale e4m3_block_scale(float amax)
+{
+    I8Scale b;
+    b.s = __fdiv_rn(amax, 448.0f);
+    if (b.s >= kE4m3QuotientMinScale) {
+        b.r = __frcp_rn(b.s);
+        b.rl = __fmul_rn(__fmaf_rn(-b.s, b.r, 1.0f), b.r);
+    } else {
+        b.r = b.s > 0.0f ? -1.0f : 0.0f;  // -1: divide per element; 0: zero block
+        b.rl = 0.0f;
+    }
+    return b;
+}
+
+// |t| with the sign of x: the correction step turns x = -0 into +0, and the sign of
+// every other quotient already equals the sign of x (s > 0).
+__device__ __forceinline__ float2 with_sign_of(float2 t, float2 x)
+{
+    return make_float2(__uint_as_float((__float_as_uint(t.x) & 0x7fffffffu) | (__float_as_uint(x.x) & 0x80000000u)),
+                       __uint_as_float((__float_as_uint(t.y) & 0x7fffffffu) | (__float_as_uint(x.y) & 0x80000000u)));
+}
+
+// BF16 of fl(decode(code) * s) for eight codes of one block.
+__device__ __forceinline__ uint4 e4m3_materialize8(uint2 codes, float s)
+{
+    float2 d[4];
+    e4m3x8_to_f32(codes, s, d);
+    return f32x8_to_bf16x8(d);
+}
+
+// Eight values of one block -> eight E4M3 codes (value i in byte i).
+__device__ __forceinline__ uint2 e4m3_quant8(const float2 (&v)[4], const I8Scale &b)
+{
+    float2 t[4];
+    if (__builtin_expect(b.r > 0.0f, 1)) {
+        const float2 r = splat(b.r), rl = splat(b.rl), ns = splat(-b.s);
+#pragma unroll
+        for (int i = 0; i < 4; i++) t[i] = with_sign_of(i8_quotient2(v[i], r, rl, ns), v[i]);
+    } else if (b.r < 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) t[i] = make_float2(__fdiv_rn(v[i].x, b.s), __fdiv_rn(v[i].y, b.s));
+    } else {
+        return make_uint2(0u, 0u);  // zero block: every code 0x00
+    }
+    return f32x8_to_e4m3x8(t);
 }
 
 }  // namespace bqk

@@ -14,19 +14,6 @@
 namespace bqk {
 namespace {
 
-// Lane-held amax of each segment -> lane 2j+h holds block (2j+h)'s amax.
-template <int SEGS>
-__device__ __forceinline__ float gather_amax(const float (&m)[SEGS], int lane)
-{
-    float mine = 0.0f;
-#pragma unroll
-    for (int j = 0; j < SEGS; j++) {
-        const float g = __shfl_sync(kFull, m[j], (lane & 1) << 4);
-        if ((lane >> 1) == j) mine = g;
-    }
-    return mine;
-}
-
 // Requantize SEGS segments of FP32 values (v[j] = lane's 8 values of segment j):
 // writes the payload, the chunk's scales and, when kOut, the BF16 materialization.
 template <int SEGS, bool kTail, bool kOut>
@@ -75,56 +62,24 @@ struct I8Codec {
     {
         requant_chunk<SEGS, kTail, kOut>(v, e0, b0, nblk, lane, q, s, out);
     }
+    static __device__ __forceinline__ uint4 dequant8(uint2 q, uint32_t word, int)
+    {
+        float2 v[4];
+        i8x8_to_f32(q, v);
+        return i8_materialize8(v, __uint_as_float(word));
+    }
 };
 
 // ---------------------------------------------------------------- quantize
 template <int SEGS>
-struct QuantOp {
-    const uint16_t *__restrict__ x;
-    int8_t *__restrict__ q;
-    float *__restrict__ s;
-    int64_t nblk;
-    int lane;
-    struct In {
-        uint4 x[SEGS];
-    };
-    template <bool kTail>
-    __device__ __forceinline__ void load(In &in, int64_t c) const
-    {
-        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
-#pragma unroll
-        for (int j = 0; j < SEGS; j++)
-            in.x[j] = (!kTail || b0 + 2 * j + (lane >> 4) < nblk) ? ld_stream_v4(x + e0 + 256 * j)
-                                                                  : make_uint4(0, 0, 0, 0);
-    }
-    template <bool kTail>
-    __device__ __forceinline__ void compute(const In &in, int64_t c) const
-    {
-        float2 v[SEGS][4];
-#pragma unroll
-        for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
-        requant_chunk<SEGS, kTail, false>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s, nullptr);
-    }
-    static constexpr uint32_t kStageBytes = 512u * SEGS;  // the chunk's BF16 values
-    static_assert(kStageBytes % 16 == 0, "bulk copies move whole 16-byte units");
-    __device__ __forceinline__ void issue(int64_t c, uint32_t stage, uint32_t bar) const
-    {
-        mbar_expect_tx(bar, kStageBytes);
-        bulk_load(stage, x + c * (256 * SEGS), kStageBytes, bar);
-    }
-    __device__ __forceinline__ void load_staged(In &in, const unsigned char *stage) const
-    {
-#pragma unroll
-        for (int j = 0; j < SEGS; j++) in.x[j] = *reinterpret_cast<const uint4 *>(stage + 512 * j + 16 * lane);
-    }
-};
+using QuantI8 = QuantOp<I8Codec, SEGS>;
 
 template <int SEGS>
 __global__ void __launch_bounds__(kThreads)
 quant_i8_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
-    const QuantOp<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
+    const QuantI8<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
@@ -134,52 +89,20 @@ quant_i8_staged_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__r
 {
     pdl_begin();
     extern __shared__ __align__(128) unsigned char smem[];
-    const QuantOp<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
-    run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<QuantOp<SEGS>, STAGES>());
+    const QuantI8<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
+    run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<QuantI8<SEGS>, STAGES>());
 }
 
 // ---------------------------------------------------------------- materialize
 template <int SEGS>
-struct DequantOp {
-    const int8_t *__restrict__ q;
-    const float *__restrict__ s;
-    uint16_t *__restrict__ out;
-    int64_t nblk;
-    int lane;
-    struct In {
-        uint2 q[SEGS];
-        uint32_t sc;
-    };
-    template <bool kTail>
-    __device__ __forceinline__ void load(In &in, int64_t c) const
-    {
-        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
-#pragma unroll
-        for (int j = 0; j < SEGS; j++)
-            in.q[j] = (!kTail || b0 + 2 * j + (lane >> 4) < nblk) ? ld_stream_v2(q + e0 + 256 * j) : make_uint2(0, 0);
-        in.sc = (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) ? ld_stream_u32(s + b0 + lane) : 0u;
-    }
-    template <bool kTail>
-    __device__ __forceinline__ void compute(const In &in, int64_t c) const
-    {
-        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
-        const int half = lane >> 4;
-#pragma unroll
-        for (int j = 0; j < SEGS; j++) {
-            const float sj = __uint_as_float(__shfl_sync(kFull, in.sc, 2 * j + half));
-            float2 v[4];
-            i8x8_to_f32(in.q[j], v);
-            if (!kTail || b0 + 2 * j + half < nblk) st_v4(out + e0 + 256 * j, i8_materialize8(v, sj));
-        }
-    }
-};
+using DequantI8 = DequantOp<I8Codec, SEGS>;
 
 template <int SEGS>
 __global__ void __launch_bounds__(kThreads)
 dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk, uint16_t *__restrict__ out)
 {
     pdl_begin();
-    const DequantOp<SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
+    const DequantI8<SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<true>(op, nblk, 2 * SEGS);
 }
 
@@ -239,6 +162,17 @@ ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
+// ---------------------------------------------------------------- reduce + quantize
+template <int SEGS, int W, bool kOut>
+__global__ void __launch_bounds__(kThreads)
+reduce_quant_i8_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
+                       float *__restrict__ s, uint16_t *__restrict__ out)
+{
+    pdl_begin();
+    const ReduceQuantOp<I8Codec, SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 2 * SEGS);
+}
+
 // Segments per warp chunk for each kernel (tuned on GB300; overridable at build time).
 #ifndef BQ_SEGS_QUANT
 #define BQ_SEGS_QUANT 4
@@ -252,10 +186,14 @@ ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_
 #ifndef BQ_SEGS_HOP
 #define BQ_SEGS_HOP 4
 #endif
+#ifndef BQ_SEGS_REDUCE
+#define BQ_SEGS_REDUCE 2
+#endif
 constexpr int kSegsQuant = BQ_SEGS_QUANT;
 constexpr int kSegsDequant = BQ_SEGS_DEQUANT;
 constexpr int kSegsAccum = BQ_SEGS_ACCUM;
 constexpr int kSegsHop = BQ_SEGS_HOP;
+constexpr int kSegsReduce = BQ_SEGS_REDUCE;
 
 // Bulk-copy stages per warp (0: the kernel reads global memory directly). Measured on
 // GB300: staging pays for the ring hop (payload, BF16 and scale streams) and costs for
@@ -299,7 +237,7 @@ template <int STAGES>
 cudaError_t launch_quant_stages(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
 {
     if constexpr (STAGES > 0)  // x is 16-byte aligned by contract
-        return launch_staged<QuantOp<kSegsQuant>, STAGES>(quant_i8_staged_kernel<kSegsQuant, STAGES>,
+        return launch_staged<QuantI8<kSegsQuant>, STAGES>(quant_i8_staged_kernel<kSegsQuant, STAGES>,
                                                            chunks(nblk, kSegsQuant), st, x, nblk, q, s);
     BQK_GRID(quant_i8_kernel<kSegsQuant>, chunks(nblk, kSegsQuant));
     return launch_kernel(quant_i8_kernel<kSegsQuant>, grid, st, x, nblk, q, s);
@@ -383,6 +321,30 @@ cudaError_t launch_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint
 {
     if (out) return launch_hop_stages<kStagesHop, true>(q_in, s_in, x, nblk, q, s, out, st);
     return launch_hop_stages<kStagesHop, false>(q_in, s_in, x, nblk, q, s, nullptr, st);
+}
+
+namespace {
+template <int W, bool kOut>
+cudaError_t launch_reduce_i8_w(const Bf16List &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
+                               cudaStream_t st)
+{
+    auto kernel = reduce_quant_i8_kernel<kSegsReduce, W, kOut>;
+    BQK_GRID(kernel, chunks(nblk, kSegsReduce));
+    return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
+}
+}  // namespace
+
+// One source width per common case (1..4 at once); more sources in groups of four.
+cudaError_t launch_reduce_quant_i8(const Bf16List &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
+                                   cudaStream_t st)
+{
+    const bool o = out != nullptr;
+    switch (W) {
+    case 1: return o ? launch_reduce_i8_w<1, true>(src, W, nblk, q, s, out, st) : launch_reduce_i8_w<1, false>(src, W, nblk, q, s, out, st);
+    case 2: return o ? launch_reduce_i8_w<2, true>(src, W, nblk, q, s, out, st) : launch_reduce_i8_w<2, false>(src, W, nblk, q, s, out, st);
+    case 3: return o ? launch_reduce_i8_w<3, true>(src, W, nblk, q, s, out, st) : launch_reduce_i8_w<3, false>(src, W, nblk, q, s, out, st);
+    default: return o ? launch_reduce_i8_w<4, true>(src, W, nblk, q, s, out, st) : launch_reduce_i8_w<4, false>(src, W, nblk, q, s, out, st);
+    }
 }
 
 }  // namespace bqk

@@ -21,6 +21,11 @@ struct WireList {
 using SourceList = WireList<int8_t, float>;       // block INT8: one FP32 scale per block
 using MxSourceList = WireList<uint8_t, uint32_t>;  // MXFP8: four E8M0 bytes per block
 
+// BF16 shards of the W ranks, in rank order (the reduce of the all-gather modes).
+struct Bf16List {
+    const uint16_t *x[kMaxSources];
+};
+
 cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st);
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out,
                               cudaStream_t st);
@@ -37,6 +42,14 @@ cudaError_t launch_accum_mx(const MxSourceList &src, int W, int64_t nblk, uint8_
                             uint16_t *out, cudaStream_t st);
 cudaError_t launch_ring_hop_mx(const uint8_t *q_in, const uint32_t *s_in, const uint16_t *x, int64_t nblk,
                                uint8_t *q, uint32_t *s, uint16_t *out, cudaStream_t st);
+cudaError_t launch_quant_mx_f16(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,
+                                int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t st);
+cudaError_t launch_reduce_quant_i8(const Bf16List &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
+                                   cudaStream_t st);
+cudaError_t launch_quant_e4m3(const uint16_t *x, int64_t nblk, uint8_t *q, float *s, cudaStream_t st);
+cudaError_t launch_dequant_e4m3(const uint8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st);
+cudaError_t launch_reduce_quant_e4m3(const Bf16List &src, int W, int64_t nblk, uint8_t *q, float *s, uint16_t *out,
+                                     cudaStream_t st);
 
 // Programmatic dependent launch: every codec kernel is launched with programmatic
 // stream serialization and begins with griddepcontrol.wait, which returns once the

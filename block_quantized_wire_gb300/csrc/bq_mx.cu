@@ -4,7 +4,9 @@
 // one E8M0 scale per 32 values) and the review comment on mxfp8_scale_byte (zero
 // group -> 127, else E8M0 of amax/448 rounded toward +inf, saturating). Slices follow
 // "[II] Support staged MXFP8 linear inputs", Behavior and Compatibility: a slice of
-// 128-column-aligned width written at a 128-column-aligned offset of a wider buffer.
+// 128-column-aligned width written at a 128-column-aligned offset of a wider buffer;
+// the same page's Behavior accepts BF16 or FP16 slices (FP16 widens exactly to binary32
+// and the rules are unchanged).
 //
 // A "block" here is 128 consecutive columns of one row (four MX groups), so the
 // warp decomposition of bq_device.cuh applies unchanged: a half-warp holds a block,
@@ -55,7 +57,7 @@ __device__ __forceinline__ int64_t block_offset(const ChunkPos &p, int k, int64_
 // block) and computes that group's E8M0 byte and multiplier 2^(127-e) once; each lane
 // then fetches its own group's multiplier per segment, and lanes 4b (b = 0..7) store
 // block b's four scale bytes as one 32-bit word.
-template <bool kTail, bool kOneRow>
+template <bool kF16, bool kTail, bool kOneRow>
 __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
                                                int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
                                                uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
@@ -73,7 +75,10 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
     float gmax = 0.0f;
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
-        bf16x8_to_f32(raw[j], v[j]);
+        if (kF16)
+            f16x8_to_f32(raw[j], v[j]);
+        else
+            bf16x8_to_f32(raw[j], v[j]);
         float m = amax8(v[j]);
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
@@ -100,16 +105,16 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
         st_u32(s + block_offset<kOneRow>(pos, lane >> 2, bpr, ld_s, 4), word);
 }
 
-template <bool kTail>
+template <bool kF16, bool kTail>
 __device__ __forceinline__ void quant_mx_chunk_any(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
                                                    int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
                                                    uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
                                                    int lane)
 {
     if (pos.cb0 + kChunkBlocks <= bpr)
-        quant_mx_chunk<kTail, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
+        quant_mx_chunk<kF16, kTail, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
     else
-        quant_mx_chunk<kTail, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
+        quant_mx_chunk<kF16, kTail, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
 }
 
 // Grid-stride walk over chunks with the chunk's (row, column block) advanced
@@ -143,6 +148,8 @@ struct ChunkWalk {
     }
 };
 
+// kF16: the input is FP16 instead of BF16.
+template <bool kF16>
 __global__ void __launch_bounds__(kThreads)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
                 int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s)
@@ -151,9 +158,10 @@ quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
     ChunkWalk w(bpr);
-    for (; w.c < nfull; w.next()) quant_mx_chunk_any<false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+    for (; w.c < nfull; w.next())
+        quant_mx_chunk_any<kF16, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
     if (w.c == nfull && nblk % kChunkBlocks)
-        quant_mx_chunk_any<true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+        quant_mx_chunk_any<kF16, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
 }
 
 template <bool kTail, bool kOneRow>
@@ -223,8 +231,16 @@ cudaError_t launch_quant_mx(const uint16_t *x, int64_t ld_x, int64_t rows, int64
                             uint8_t *s, int64_t ld_s, cudaStream_t st)
 {
     const int64_t bpr = cols / 128, nblk = rows * bpr;
-    BQK_GRID(quant_mx_kernel, (nblk + kChunkBlocks - 1) / kChunkBlocks);
-    return launch_kernel(quant_mx_kernel, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
+    BQK_GRID(quant_mx_kernel<false>, (nblk + kChunkBlocks - 1) / kChunkBlocks);
+    return launch_kernel(quant_mx_kernel<false>, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
+}
+
+cudaError_t launch_quant_mx_f16(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q, int64_t ld_q,
+                                uint8_t *s, int64_t ld_s, cudaStream_t st)
+{
+    const int64_t bpr = cols / 128, nblk = rows * bpr;
+    BQK_GRID(quant_mx_kernel<true>, (nblk + kChunkBlocks - 1) / kChunkBlocks);
+    return launch_kernel(quant_mx_kernel<true>, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
 }
 
 cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_s, int64_t rows,

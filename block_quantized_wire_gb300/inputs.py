@@ -109,13 +109,17 @@ def prefill_65536(device="cuda", rows: int = 65536, cols: int = HIDDEN, W: int =
     return [prefill_buffer(w, device, rows, cols, seed0) for w in range(W)]
 
 
-def mx_slices_4096(device="cuda", rows: int = 4096, cols: int = HIDDEN, n_slices: int = 6, seed0: int = 5101):
+def mx_slices_4096(device="cuda", rows: int = 4096, cols: int = HIDDEN, n_slices: int = 6, seed0: int = 5101,
+                   dtype: torch.dtype = torch.bfloat16):
+    """The staged MX slices; dtype torch.float16 gives the FP16 slices the staged-input
+    page also accepts (the same FP32 draws, rounded once to FP16; they stay far inside
+    the FP16 range)."""
     out = []
     for i in range(n_slices):
         g = _gen(seed0 + i, device)
         x = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(0.02)
         x = _with_outliers(x, g, 0.001, 100.0)
-        out.append(x.to(torch.bfloat16))
+        out.append(x.to(dtype))
     return out
 
 

@@ -14,6 +14,10 @@ topology the owner materializes from the same final payload it forwards.
 
 From "feat(pcie_dma): add INT8 and MXFP8 wire modes", Summary: ``mx``, ``mx_ring`` and
 ``mx_a2a`` are the same topologies with the MXFP8 codec on flat MX wires.
+
+``i8_ag`` and ``e4m3_ag`` are the all-gather modes whole: for every shard, its owner
+reduces the W ranks' BF16 copies (binary32 in rank order, one rounding to BF16) and
+quantizes the result in the same kernel; every rank then materializes all W payloads.
 """
 from __future__ import annotations
 
@@ -131,3 +135,38 @@ def mx_a2a(xs, stream=None):
 
 def mx_ring(xs, stream=None):
     return ring(MX, xs, stream)
+
+
+def _allgather(reduce_quant, empty, dequant, xs, stream=None):
+    """BF16 reduce-scatter fused with quantization, then the quantized all-gather.
+    Returns (per-rank BF16 outputs, payload (q, s) per shard, owner BF16 per shard)."""
+    W = len(xs)
+    rows = xs[0].shape[0]
+    if rows % W:
+        raise ValueError("all-gather mode: rows must divide evenly into W shards")
+    sr = rows // W
+    n = xs[0][:sr].numel()
+    finals, owners = [], []
+    for c in range(W):
+        _, q, s = empty(n, xs[0].device)
+        owner = torch.empty_like(xs[0][c * sr:(c + 1) * sr])
+        reduce_quant([x[c * sr:(c + 1) * sr] for x in xs], q, s, owner, stream)
+        finals.append((q, s))
+        owners.append(owner)
+    outs = []
+    for _rank in range(W):
+        out = torch.empty_like(xs[0])
+        for c in range(W):
+            dequant(finals[c][0], finals[c][1], out[c * sr:(c + 1) * sr], stream)
+        outs.append(out)
+    return outs, finals, owners
+
+
+def i8_ag(xs, stream=None):
+    """The ``i8`` mode: BF16 reduce-scatter + INT8 all-gather."""
+    return _allgather(codec.reduce_quant_i8, codec.empty_wire_i8, codec.dequant_i8, xs, stream)
+
+
+def e4m3_ag(xs, stream=None):
+    """The E4M3 all-gather mode with the legacy E4M3 codec."""
+    return _allgather(codec.reduce_quant_e4m3, codec.empty_wire_e4m3, codec.dequant_e4m3, xs, stream)

@@ -43,6 +43,12 @@
  *              acc = (((d_0 + d_1) + d_2) + ...) in binary32 in source order; acc is
  *              requantized per 32-value group with the MX scale and value rules,
  *              the amax taken over the binary32 sums.
+ *   reduce + quantize  (the all-gather modes' BF16 reduce-scatter fused with the
+ *              payload) y = BF16_rne(((x_0 + x_1) + ...) in binary32 in rank
+ *              order), then y is quantized by the codec.
+ *   legacy E4M3  s = fl(amax / 448) per 128-value block; code =
+ *              E4M3_rne_satfinite(fl(x / s)), sign of zero kept; a block with s == 0
+ *              has every code 0x00; materialize out = BF16_rne(fl(decode(code) * s)).
  *   MX ring hop  v = fl(decode(code_in) * 2^(e_in-127) + x_local), requantized as
  *              MX. (The MXFP8 page's Summary runs its codec on the same ring and
  *              all-to-all topologies, mx_ring and mx_a2a; these two rules are the
@@ -89,7 +95,7 @@ extern "C" {
 #define BQ_API
 #endif
 
-#define BQ_ABI_VERSION 2
+#define BQ_ABI_VERSION 3
 #define BQ_BLOCK_I8 128 /* values per INT8 block */
 #define BQ_GROUP_MX 32  /* values per E8M0 scale */
 #define BQ_MAX_W 16     /* most sources one accumulate call takes */
@@ -200,6 +206,41 @@ BQ_API bq_status bq_dequant_accum_mx(const uint8_t *const *q_srcs, const uint8_t
 BQ_API bq_status bq_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const void *x_local_bf16,
                          int64_t n, uint8_t *q_out, uint8_t *s_out, void *out_bf16,
                          cudaStream_t stream);
+
+/* bq_quant_mx for an FP16 input ("[II] Support staged MXFP8 linear inputs", Behavior:
+ * BF16 or FP16 feature slices). FP16 widens exactly to binary32; the arguments,
+ * layout and rules are those of bq_quant_mx with x_f16 in place of x_bf16. */
+BQ_API bq_status bq_quant_mx_f16(const void *x_f16, int64_t rows, int64_t cols, int64_t ld_x,
+                          uint8_t *q_e4m3, int64_t ld_q, uint8_t *s_e8m0, int64_t ld_s,
+                          cudaStream_t stream);
+
+/* The i8 mode's BF16 reduce-scatter fused with its INT8 all-gather payload
+ * ("feat(pcie_dma): add block-INT8 wire modes for AG, ring, and A2A", Summary: i8 =
+ * BF16 reduce-scatter + INT8 all-gather): per element the W ranks' BF16 values are
+ * added in rank order in binary32 and rounded once to BF16; that BF16 shard is
+ * quantized as by bq_quant_i8, without writing it to memory.
+ *   x_srcs     HOST array of W DEVICE pointers to [n] BF16 (16-byte aligned), rank order
+ *   W          1 <= W <= BQ_MAX_W
+ *   q, scales  [n] int8 payload, [n/128] FP32 scales (written)
+ *   out_bf16   NULL, or [n] BF16 materialization of the payload (the owner's copy).
+ * Sources may repeat or overlap one another. */
+BQ_API bq_status bq_reduce_quant_i8(const void *const *x_srcs, int W, int64_t n, int8_t *q,
+                             float *scales, void *out_bf16, cudaStream_t stream);
+
+/* BF16 -> legacy E4M3 wire (same page, Summary and Why: the E4M3 codec keeps one E4M3
+ * byte per value and one FP32 scale per 128 values, 132 bytes per block).
+ *   x_bf16 [n] (read), q [n] E4M3 codes (written, 16-byte aligned), scales [n/128]
+ *   FP32 (written, 4-byte aligned). */
+BQ_API bq_status bq_quant_e4m3(const void *x_bf16, int64_t n, uint8_t *q, float *scales,
+                        cudaStream_t stream);
+
+/* Legacy E4M3 wire -> BF16: out = BF16_rne(fl(decode(code) * s)). */
+BQ_API bq_status bq_dequant_e4m3(const uint8_t *q, const float *scales, int64_t n, void *out_bf16,
+                          cudaStream_t stream);
+
+/* bq_reduce_quant_i8 with the legacy E4M3 codec (the E4M3 all-gather mode). */
+BQ_API bq_status bq_reduce_quant_e4m3(const void *const *x_srcs, int W, int64_t n, uint8_t *q,
+                               float *scales, void *out_bf16, cudaStream_t stream);
 
 /* Number of bounded waits inside codec kernels that ran out since the previous call;
  * the count is reset to 0. Kernels that stage their inputs through shared memory wait

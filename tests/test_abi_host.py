@@ -26,7 +26,8 @@ def declared_functions():
 def test_header_declares_the_calls():
     names = declared_functions()
     for want in ("bq_quant_i8", "bq_dequant_i8", "bq_dequant_accum_i8", "bq_ring_hop_i8", "bq_quant_mx",
-                 "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_wire_bytes", "bq_status_string",
+                 "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_quant_mx_f16", "bq_reduce_quant_i8",
+                 "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_wire_bytes", "bq_status_string",
                  "bq_abi_version", "bq_take_wait_timeouts", "bq_selftest_wait_timeout"):
         assert want in names
 
@@ -34,7 +35,7 @@ def test_header_declares_the_calls():
 def test_library_exports_every_declared_symbol(bq_lib):
     for name in declared_functions():
         assert hasattr(bq_lib, name), name
-    assert bq_lib.bq_abi_version() == 2
+    assert bq_lib.bq_abi_version() == 3
 
 
 def test_wire_bytes_and_status_strings(bq_lib):
@@ -152,6 +153,55 @@ def test_ring_hop_mx_rejections(bq_lib):
     assert f(qi, si, x, n, x + 2 * n - 16, so, None, None) == ALIAS
     assert f(qi, si, x, n, qo, si + n // 32 - 4, None, None) == ALIAS
     assert f(qi, si, x, n, qo, so, qo + n - 16, None) == ALIAS
+
+
+@pytest.mark.parametrize("name", ["bq_reduce_quant_i8", "bq_reduce_quant_e4m3"])
+def test_reduce_quant_rejections(bq_lib, name):
+    f = getattr(bq_lib, name)
+    n = 4096
+    x = [A + k * 0x100000 for k in range(4)]
+    xp, xa = _srcs(x)
+    q, s, o = A + 0x2000000, A + 0x3000000, A + 0x4000000
+    assert f(xp, 0, n, q, s, None, None) == SHAPE
+    assert f(xp, 17, n, q, s, None, None) == SHAPE
+    assert f(xp, 4, n + 64, q, s, None, None) == SHAPE
+    assert f(xp, 4, 0, q, s, None, None) == OK
+    assert f(None, 4, n, q, s, None, None) == NULL
+    xn, xna = _srcs([x[0], x[1], None, x[3]])
+    assert f(xn, 4, n, q, s, None, None) == NULL
+    xm, xma = _srcs([x[0], x[1] + 2, x[2], x[3]])
+    assert f(xm, 4, n, q, s, None, None) == ALIGN
+    assert f(xp, 4, n, q + 8, s, None, None) == ALIGN
+    assert f(xp, 4, n, q, s + 2, None, None) == ALIGN
+    assert f(xp, 4, n, q, s, o + 8, None) == ALIGN
+    assert f(xp, 4, n, x[3] + 2 * n - 16, s, None, None) == ALIAS  # payload over a source
+    assert f(xp, 4, n, q, s, q + n - 16, None) == ALIAS
+
+
+def test_e4m3_rejections(bq_lib):
+    fq, fd = bq_lib.bq_quant_e4m3, bq_lib.bq_dequant_e4m3
+    n = 1024
+    assert fq(A, 100, A + 0x100000, A + 0x200000, None) == SHAPE
+    assert fq(None, 0, None, None, None) == OK
+    assert fq(A, n, None, A + 0x200000, None) == NULL
+    assert fq(A, n, A + 0x100004, A + 0x200000, None) == ALIGN
+    assert fq(A, n, A + 0x100000, A + 0x200001, None) == ALIGN
+    assert fq(A, n, A + 512, A + 0x200000, None) == ALIAS
+    assert fd(A, A + 0x100000, 129, A + 0x200000, None) == SHAPE
+    assert fd(A, A + 0x100000, n, None, None) == NULL
+    assert fd(A, A + 0x100000, n, A + 0x200004, None) == ALIGN
+    assert fd(A, A + 0x100000, n, A + 0x100000 - 16, None) == ALIAS
+
+
+def test_quant_mx_f16_rejections(bq_lib):
+    f = bq_lib.bq_quant_mx_f16
+    assert f(A, 4, 100, 100, A + 0x100000, 100, A + 0x200000, 4, None) == SHAPE
+    assert f(A, 4, 128, 64, A + 0x100000, 128, A + 0x200000, 4, None) == SHAPE  # ld_x < cols
+    assert f(A, 0, 128, 128, None, 128, None, 4, None) == OK
+    assert f(None, 4, 128, 128, A + 0x100000, 128, A + 0x200000, 4, None) == NULL
+    assert f(A + 2, 4, 128, 128, A + 0x100000, 128, A + 0x200000, 4, None) == ALIGN
+    assert f(A, 4, 128, 132, A + 0x100000, 128, A + 0x200000, 4, None) == ALIGN  # ld_x % 8
+    assert f(A, 4, 128, 128, A + 512, 128, A + 0x200000, 4, None) == ALIAS
 
 
 def test_mx_rejections(bq_lib):

@@ -25,6 +25,10 @@ def test_algorithmic_bytes_per_launch():
     assert bench.kernel_bytes("dequant_mx", 4096 * 43008) == 533987328
     assert bench.kernel_bytes("dequant_accum_mx", n) == 2422210560  # same wire size as INT8
     assert bench.kernel_bytes("ring_hop_mx", n) == 1908408320
+    assert bench.kernel_bytes("reduce_quant_i8", n) == 4 * 2 * n + 484442112  # four BF16 shards in, one wire out
+    assert bench.kernel_bytes("reduce_quant_e4m3", n) == bench.kernel_bytes("reduce_quant_i8", n)
+    assert bench.kernel_bytes("quant_e4m3", n) == bench.kernel_bytes("quant_i8", n)
+    assert bench.kernel_bytes("quant_mx_f16", 4096 * 7168) == 88997888
     step = (4 * 1423966208 + 2422210560 + 1423966208 + 1908408320 + 6 * 88997888 + 533987328)
     assert step == 12518424576
 
