@@ -223,14 +223,20 @@ class ClockSampler:
 class Pipeline:
     """Device buffers and launch list of one codec step (caller-owned memory)."""
 
-    def __init__(self, rows: int, slice_rows: int, device):
+    def __init__(self, rows: int, slice_rows: int, device, generate: bool = True):
         from block_quantized_wire_gb300 import codec, inputs
         self.codec = codec
+        self.device = device
         self.rows, self.slice_rows = rows, slice_rows
         self.n = rows * HIDDEN
         self.n_slice = slice_rows * HIDDEN
-        self.xs = [inputs.prefill_buffer(w, device=device, rows=rows) for w in range(W_SRC)]
-        self.slices = inputs.mx_slices_4096(device=device, rows=slice_rows)
+        if generate:
+            self.xs = [inputs.prefill_buffer(w, device=device, rows=rows) for w in range(W_SRC)]
+            self.slices = inputs.mx_slices_4096(device=device, rows=slice_rows)
+        else:  # buffers only; the inputs arrive by copy
+            self.xs = [torch.empty((rows, HIDDEN), dtype=torch.bfloat16, device=device) for _ in range(W_SRC)]
+            self.slices = [torch.empty((slice_rows, HIDDEN), dtype=torch.bfloat16, device=device)
+                           for _ in range(N_SLICES)]
         self.wires = [codec.empty_wire_i8(self.n, device) for _ in range(W_SRC)]
         self.acc = codec.empty_wire_i8(self.n, device)
         self.hop = codec.empty_wire_i8(self.n, device)
@@ -272,26 +278,74 @@ class Pipeline:
             if events is not None:
                 events[i].record()
 
-    # end-to-end: host inputs in, host results out
-    def host_buffers(self):
-        pin = dict(pin_memory=True)
-        self.h_xs = [torch.empty_like(x, device="cpu", **pin).copy_(x) for x in self.xs]
-        self.h_slices = [torch.empty_like(x, device="cpu", **pin).copy_(x) for x in self.slices]
-        self.h_results = [torch.empty_like(t, device="cpu", **pin) for t in self.results()]
-        self.h2d = sum(t.numel() * t.element_size() for t in self.h_xs + self.h_slices)
-        self.d2h = sum(t.numel() * t.element_size() for t in self.h_results)
-
     def results(self):
         return [self.acc[0], self.out, self.hop[0], self.mx_q, self.mx_s, self.mx_out]
 
-    def run_e2e(self):
-        for d, h in zip(self.xs, self.h_xs):
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(self.slices, self.h_slices):
-            d.copy_(h, non_blocking=True)
-        self.run()
-        for h, d in zip(self.h_results, self.results()):
-            h.copy_(d, non_blocking=True)
+
+class EndToEnd:
+    """The step through the public API from host memory: every step copies its inputs
+    from pinned host buffers to the device and its results back to pinned host buffers.
+    Two device buffer sets alternate between consecutive steps. The copies of both
+    directions run in order on one copy stream (step k+1's inputs, then step k's
+    results) and the codec launches on a second stream, so a step's computation hides
+    behind the copies of its neighbours. Running the two copy directions at once was
+    slower on GB300's shared host link than running them back to back. Events order
+    the reuse of each buffer set: its inputs are overwritten only after the step that
+    read them has computed, and its results only after they have been copied out."""
+
+    def __init__(self, pipe: Pipeline):
+        self.sets = [pipe, Pipeline(pipe.rows, pipe.slice_rows, pipe.device, generate=False)]
+        pin = dict(pin_memory=True)
+        self.h_xs = [torch.empty_like(x, device="cpu", **pin).copy_(x) for x in pipe.xs]
+        self.h_slices = [torch.empty_like(x, device="cpu", **pin).copy_(x) for x in pipe.slices]
+        self.h_results = [torch.empty_like(t, device="cpu", **pin) for t in pipe.results()]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_xs + self.h_slices)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_results)
+        self.s_copy, self.s_comp = torch.cuda.Stream(), torch.cuda.Stream()
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.comp_done = [torch.cuda.Event() for _ in range(2)]
+
+    def _copy_in(self, k: int):
+        i = k % 2
+        p = self.sets[i]
+        with torch.cuda.stream(self.s_copy):
+            if k >= 2:
+                self.s_copy.wait_event(self.comp_done[i])  # step k-2 has read this set's inputs
+            for d, h in zip(p.xs, self.h_xs):
+                d.copy_(h, non_blocking=True)
+            for d, h in zip(p.slices, self.h_slices):
+                d.copy_(h, non_blocking=True)
+            self.in_ready[i].record(self.s_copy)
+
+    def _compute(self, k: int):
+        i = k % 2
+        with torch.cuda.stream(self.s_comp):
+            # inputs are in; step k-2's results were copied out earlier on the copy
+            # stream, before this step's inputs, so in_ready covers both
+            self.s_comp.wait_event(self.in_ready[i])
+            self.sets[i].run()
+            self.comp_done[i].record(self.s_comp)
+
+    def _copy_out(self, k: int):
+        i = k % 2
+        with torch.cuda.stream(self.s_copy):
+            self.s_copy.wait_event(self.comp_done[i])
+            for h, d in zip(self.h_results, self.sets[i].results()):
+                h.copy_(d, non_blocking=True)
+
+    def run(self, nsteps: int):
+        cur = torch.cuda.current_stream()
+        for st in (self.s_copy, self.s_comp):
+            st.wait_stream(cur)
+        # copy stream order: in(0), in(1), out(0), in(2), out(1), ..., out(n-1)
+        for k in range(nsteps):
+            self._copy_in(k)
+            self._compute(k)
+            if k >= 1:
+                self._copy_out(k - 1)
+        self._copy_out(nsteps - 1)
+        for st in (self.s_copy, self.s_comp):
+            cur.wait_stream(st)
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -481,23 +535,25 @@ def run_bq(args, rank, world, local):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        pipe.host_buffers()
-        pipe.run_e2e()
+        ee = EndToEnd(pipe)
+        ee.run(2)
         torch.cuda.synchronize()
         n_e2e = max(2, min(args.steps, args.e2e_steps))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         e0.record()
-        for _ in range(n_e2e):
-            pipe.run_e2e()
+        ee.run(n_e2e)
         e1.record()
         torch.cuda.synchronize()
         barrier(world)
         e_ms = max_over_ranks(e0.elapsed_time(e1), world) / n_e2e
         e2e = {"value": round(world * step_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
-               "h2d_bytes_per_step": pipe.h2d, "d2h_bytes_per_step": pipe.d2h, "ms_per_step": round(e_ms, 3),
-               "steps": n_e2e}
+               "h2d_bytes_per_step": ee.h2d, "d2h_bytes_per_step": ee.d2h, "ms_per_step": round(e_ms, 3),
+               "steps": n_e2e,
+               "overlap": "two device buffer sets; both copy directions in order on one stream, codec launches "
+                          "on another, so each step's computation overlaps its neighbours' copies"}
+        del ee
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -56,8 +56,12 @@ struct E4m3Codec {
     }
 };
 
+#ifndef BQ_QUANT_E4M3_MIN_CTAS
+#define BQ_QUANT_E4M3_MIN_CTAS 4
+#endif
+
 template <int SEGS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, BQ_QUANT_E4M3_MIN_CTAS)
 quant_e4m3_kernel(const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();

@@ -148,9 +148,13 @@ struct ChunkWalk {
     }
 };
 
+#ifndef BQ_QUANT_MX_MIN_CTAS
+#define BQ_QUANT_MX_MIN_CTAS 3
+#endif
+
 // kF16: the input is FP16 instead of BF16.
 template <bool kF16>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, BQ_QUANT_MX_MIN_CTAS)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
                 int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s)
 {

@@ -115,3 +115,26 @@ def test_bounded_waits_do_not_run_out_and_can_be_observed():
     assert codec.take_wait_timeouts() == 0
     q, s, out = topology.i8_roundtrip(xs[0])
     assert torch.isfinite(out.float()).all()
+
+
+def test_end_to_end_pipeline_copies_back_the_device_results():
+    # the benchmark's host-to-host leg (two buffer sets, three streams, overlapped
+    # steps) delivers exactly the results of a plain device step on the same inputs
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    pipe = bench.Pipeline(1024, 256, torch.device("cuda", 0))
+    pipe.run()
+    torch.cuda.synchronize()
+    want = [t.clone() for t in pipe.results()]
+    ee = bench.EndToEnd(pipe)
+    for t in pipe.results():
+        t.zero_()
+    ee.run(5)
+    torch.cuda.synchronize()
+    for h, w in zip(ee.h_results, want):
+        assert torch.equal(h, w.cpu())
+    for p in ee.sets:  # both buffer sets computed the same step
+        for t, w in zip(p.results(), want):
+            assert torch.equal(t, w)
