@@ -15,7 +15,7 @@ from . import build as _build
 _lock = threading.Lock()
 _lib = None
 
-ABI_VERSION = 3
+ABI_VERSION = 4
 BQ_OK = 0
 STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_ALIAS",
                 5: "BQ_ERR_CUDA"}
@@ -35,6 +35,8 @@ _PROTOS = {
     "bq_dequant_accum_mx": ([_P, _P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_ring_hop_mx": ([_P, _P, _P, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_quant_mx_f16": ([_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
+    "bq_quant_mx_tiled": ([_P, ctypes.c_int, _I64, _I64, _I64, _P, _I64, _P, _I64, _I64, _P], ctypes.c_int),
+    "bq_mx_tiled_scale_bytes": ([_I64, _I64], _I64),
     "bq_reduce_quant_i8": ([_P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_quant_e4m3": ([_P, _I64, _P, _P, _P], ctypes.c_int),
     "bq_dequant_e4m3": ([_P, _P, _I64, _P, _P], ctypes.c_int),

@@ -169,6 +169,32 @@ def dequant_mx(q: torch.Tensor, s: torch.Tensor, out: torch.Tensor, stream=None)
     check("bq_dequant_mx", load().bq_dequant_mx(qp, ld_q, sp, ld_s, rows, cols, op, ld_o, _stream(stream)))
 
 
+def mx_tiled_scale_bytes(rows: int, g_total: int) -> int:
+    """Bytes of the tiled GEMM scale layout for rows x g_total E8M0 scales."""
+    r = load().bq_mx_tiled_scale_bytes(rows, g_total)
+    if r < 0:
+        raise ValueError(f"mx_tiled_scale_bytes: g_total={g_total} is not a non-negative multiple of 4")
+    return r
+
+
+def quant_mx_tiled(x: torch.Tensor, q: torch.Tensor, s_tiled: torch.Tensor, g_total: int, g0: int = 0,
+                   stream=None) -> None:
+    """BF16 or FP16 x [rows, cols] -> E4M3 q [rows, cols] and E8M0 scales written into the
+    tiled GEMM layout of a tensor with g_total scale columns, starting at scale column g0
+    (the slice's column offset / 32). Parity of the layout itself is unpinned: the pages
+    do not print it (include/bq.h, bq_quant_mx_tiled)."""
+    f16 = x.dtype == torch.float16
+    xp, rows, cols, ld_x = _rows(x, torch.float16 if f16 else torch.bfloat16, "x")
+    qp, qr, qc, ld_q = _rows(q, torch.uint8, "q")
+    if (qr, qc) != (rows, cols):
+        raise ValueError("quant_mx_tiled: q's shape does not match x")
+    if s_tiled.numel() < mx_tiled_scale_bytes(rows, g_total):
+        raise ValueError("quant_mx_tiled: the tiled scale buffer is too small")
+    check("bq_quant_mx_tiled", load().bq_quant_mx_tiled(
+        xp, int(f16), rows, cols, ld_x, qp, ld_q, _flat(s_tiled, torch.uint8, "s_tiled"), g_total, g0,
+        _stream(stream)))
+
+
 # ---------------------------------------------------------------- flat MXFP8 wires
 def quant_mx_flat(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
     """BF16 x [n] -> flat MX wire q [n] + s [n/32] (bq_quant_mx on one row of n values)."""

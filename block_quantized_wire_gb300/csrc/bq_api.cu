@@ -290,6 +290,29 @@ bq_status bq_quant_mx_f16(const void *x_f16, int64_t rows, int64_t cols, int64_t
                                               s_e8m0, ld_s, stream));
 }
 
+bq_status bq_quant_mx_tiled(const void *x, int x_is_f16, int64_t rows, int64_t cols, int64_t ld_x, uint8_t *q_e4m3,
+                            int64_t ld_q, uint8_t *s_tiled, int64_t g_total, int64_t g0, cudaStream_t stream)
+{
+    if (rows < 0 || cols < 0 || cols % 128) return BQ_ERR_SHAPE;
+    if (g_total < 0 || g_total % 4 || g0 < 0 || g0 % 4 || g0 + cols / BQ_GROUP_MX > g_total) return BQ_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return BQ_OK;
+    if (ld_x < cols || ld_q < cols) return BQ_ERR_SHAPE;
+    if (!x || !q_e4m3 || !s_tiled) return BQ_ERR_NULL;
+    if (!aligned(x, 16) || ld_x % 8 || !aligned(q_e4m3, 16) || ld_q % 16 || !aligned(s_tiled, 4)) return BQ_ERR_ALIGN;
+    const int64_t tiled_bytes = ((rows + 127) / 128) * (g_total / 4) * 512;
+    const Range ins[] = {span2d(x, rows, 2 * cols, 2 * ld_x)};
+    const Range outs[] = {span2d(q_e4m3, rows, cols, ld_q), span(s_tiled, tiled_bytes)};
+    if (any_alias(outs, 2, ins, 1)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_quant_mx_tiled(static_cast<const uint16_t *>(x), x_is_f16 != 0, ld_x, rows, cols,
+                                                q_e4m3, ld_q, s_tiled, g_total / 4, g0 / 4, stream));
+}
+
+int64_t bq_mx_tiled_scale_bytes(int64_t rows, int64_t g_total)
+{
+    if (rows < 0 || g_total < 0 || g_total % 4) return -1;
+    return ((rows + 127) / 128) * (g_total / 4) * 512;
+}
+
 namespace {
 // Shared checks of the reduce + quantize calls: W BF16 sources -> payload [n] (1 byte
 // per value, 16-byte aligned), FP32 scales [n/128] (4-byte aligned), optional BF16.

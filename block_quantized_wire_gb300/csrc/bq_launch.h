@@ -44,6 +44,8 @@ cudaError_t launch_ring_hop_mx(const uint8_t *q_in, const uint32_t *s_in, const 
                                uint8_t *q, uint32_t *s, uint16_t *out, cudaStream_t st);
 cudaError_t launch_quant_mx_f16(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,
                                 int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t st);
+cudaError_t launch_quant_mx_tiled(const uint16_t *x, bool f16, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,
+                                  int64_t ld_q, uint8_t *s_tiled, int64_t tiles_per_row, int64_t c0, cudaStream_t st);
 cudaError_t launch_reduce_quant_i8(const Bf16List &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                                    cudaStream_t st);
 cudaError_t launch_quant_e4m3(const uint16_t *x, int64_t nblk, uint8_t *q, float *s, cudaStream_t st);

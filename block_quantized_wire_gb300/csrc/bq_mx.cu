@@ -51,17 +51,36 @@ __device__ __forceinline__ int64_t block_offset(const ChunkPos &p, int k, int64_
     return r * ld + c * wid;
 }
 
+// Byte offset of the four scale bytes of block k of the chunk. Row-major: row * ld_s +
+// 4 * (block column). kTiled: the tiled layout of block-scaled GEMM operands, where a
+// 128-value block's four E8M0 bytes are one row of a 128-row x 4-column tile; ld_s is
+// then the number of tiles per tile row (scale columns of the whole tensor / 4) and c0
+// the slice's first tile column. Inside a tile, row r sits at (r % 32) * 16 + (r / 32) * 4.
+template <bool kOneRow, bool kTiled>
+__device__ __forceinline__ int64_t scale_offset(const ChunkPos &p, int k, int64_t bpr, int64_t ld_s, int64_t c0)
+{
+    if (!kTiled) return block_offset<kOneRow>(p, k, bpr, ld_s, 4);
+    int64_t r, cb;
+    if (kOneRow) {
+        r = p.row0;
+        cb = p.cb0 + k;
+    } else {
+        advance(p.row0, p.cb0, k, bpr, r, cb);
+    }
+    return ((r >> 7) * ld_s + c0 + cb) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+}
+
 // One warp chunk = 4 segments = 8 blocks = 32 groups of 32 values. After the group
 // amaxes are reduced (4 lanes per group), lane L gathers the amax of the chunk's group
 // L (group order = scale-byte order within the chunk: block-major, 4 groups per
 // block) and computes that group's E8M0 byte and multiplier 2^(127-e) once; each lane
 // then fetches its own group's multiplier per segment, and lanes 4b (b = 0..7) store
 // block b's four scale bytes as one 32-bit word.
-template <bool kF16, bool kTail, bool kOneRow>
+template <bool kF16, bool kTiled, bool kTail, bool kOneRow>
 __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
                                                int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
-                                               uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
-                                               int lane)
+                                               uint8_t *__restrict__ s, int64_t ld_s, int64_t c0, int64_t b0,
+                                               ChunkPos pos, int lane)
 {
     constexpr int SEGS = kSegs;
     const int half = lane >> 4, hl = lane & 15;
@@ -102,19 +121,19 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
     if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk))
-        st_u32(s + block_offset<kOneRow>(pos, lane >> 2, bpr, ld_s, 4), word);
+        st_u32(s + scale_offset<kOneRow, kTiled>(pos, lane >> 2, bpr, ld_s, c0), word);
 }
 
-template <bool kF16, bool kTail>
+template <bool kF16, bool kTiled, bool kTail>
 __device__ __forceinline__ void quant_mx_chunk_any(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
                                                    int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
-                                                   uint8_t *__restrict__ s, int64_t ld_s, int64_t b0, ChunkPos pos,
-                                                   int lane)
+                                                   uint8_t *__restrict__ s, int64_t ld_s, int64_t c0, int64_t b0,
+                                                   ChunkPos pos, int lane)
 {
     if (pos.cb0 + kChunkBlocks <= bpr)
-        quant_mx_chunk<kF16, kTail, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
+        quant_mx_chunk<kF16, kTiled, kTail, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, b0, pos, lane);
     else
-        quant_mx_chunk<kF16, kTail, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, b0, pos, lane);
+        quant_mx_chunk<kF16, kTiled, kTail, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, b0, pos, lane);
 }
 
 // Grid-stride walk over chunks with the chunk's (row, column block) advanced
@@ -152,20 +171,21 @@ struct ChunkWalk {
 #define BQ_QUANT_MX_MIN_CTAS 3
 #endif
 
-// kF16: the input is FP16 instead of BF16.
-template <bool kF16>
+// kF16: the input is FP16 instead of BF16. kTiled: scales go to the tiled GEMM layout
+// (see scale_offset), c0 the slice's first tile column.
+template <bool kF16, bool kTiled>
 __global__ void __launch_bounds__(kThreads, BQ_QUANT_MX_MIN_CTAS)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
-                int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s)
+                int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s, int64_t c0)
 {
     pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
     ChunkWalk w(bpr);
     for (; w.c < nfull; w.next())
-        quant_mx_chunk_any<kF16, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+        quant_mx_chunk_any<kF16, kTiled, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
     if (w.c == nfull && nblk % kChunkBlocks)
-        quant_mx_chunk_any<kF16, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, w.b0, w.pos, lane);
+        quant_mx_chunk_any<kF16, kTiled, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
 }
 
 template <bool kTail, bool kOneRow>
@@ -231,20 +251,35 @@ dequant_mx_kernel(const uint8_t *__restrict__ q, int64_t ld_q, const uint8_t *__
 
 }  // namespace
 
+namespace {
+template <bool kF16, bool kTiled>
+cudaError_t launch_quant_mx_any(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q, int64_t ld_q,
+                                uint8_t *s, int64_t ld_s, int64_t c0, cudaStream_t st)
+{
+    const int64_t bpr = cols / 128, nblk = rows * bpr;
+    auto kernel = quant_mx_kernel<kF16, kTiled>;
+    BQK_GRID(kernel, (nblk + kChunkBlocks - 1) / kChunkBlocks);
+    return launch_kernel(kernel, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0);
+}
+}  // namespace
+
 cudaError_t launch_quant_mx(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q, int64_t ld_q,
                             uint8_t *s, int64_t ld_s, cudaStream_t st)
 {
-    const int64_t bpr = cols / 128, nblk = rows * bpr;
-    BQK_GRID(quant_mx_kernel<false>, (nblk + kChunkBlocks - 1) / kChunkBlocks);
-    return launch_kernel(quant_mx_kernel<false>, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
+    return launch_quant_mx_any<false, false>(x, ld_x, rows, cols, q, ld_q, s, ld_s, 0, st);
 }
 
 cudaError_t launch_quant_mx_f16(const uint16_t *x, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q, int64_t ld_q,
                                 uint8_t *s, int64_t ld_s, cudaStream_t st)
 {
-    const int64_t bpr = cols / 128, nblk = rows * bpr;
-    BQK_GRID(quant_mx_kernel<true>, (nblk + kChunkBlocks - 1) / kChunkBlocks);
-    return launch_kernel(quant_mx_kernel<true>, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s);
+    return launch_quant_mx_any<true, false>(x, ld_x, rows, cols, q, ld_q, s, ld_s, 0, st);
+}
+
+cudaError_t launch_quant_mx_tiled(const uint16_t *x, bool f16, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,
+                                  int64_t ld_q, uint8_t *s_tiled, int64_t tiles_per_row, int64_t c0, cudaStream_t st)
+{
+    if (f16) return launch_quant_mx_any<true, true>(x, ld_x, rows, cols, q, ld_q, s_tiled, tiles_per_row, c0, st);
+    return launch_quant_mx_any<false, true>(x, ld_x, rows, cols, q, ld_q, s_tiled, tiles_per_row, c0, st);
 }
 
 cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, int64_t ld_s, int64_t rows,

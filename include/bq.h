@@ -95,7 +95,7 @@ extern "C" {
 #define BQ_API
 #endif
 
-#define BQ_ABI_VERSION 3
+#define BQ_ABI_VERSION 4
 #define BQ_BLOCK_I8 128 /* values per INT8 block */
 #define BQ_GROUP_MX 32  /* values per E8M0 scale */
 #define BQ_MAX_W 16     /* most sources one accumulate call takes */
@@ -213,6 +213,28 @@ BQ_API bq_status bq_ring_hop_mx(const uint8_t *q_in, const uint8_t *s_in, const 
 BQ_API bq_status bq_quant_mx_f16(const void *x_f16, int64_t rows, int64_t cols, int64_t ld_x,
                           uint8_t *q_e4m3, int64_t ld_q, uint8_t *s_e8m0, int64_t ld_s,
                           cudaStream_t stream);
+
+/* bq_quant_mx (BF16, or FP16 when x_is_f16 != 0) writing the E8M0 scales in the tiled
+ * layout that block-scaled GEMM operands use, for a GEMM that consumes the assembled
+ * MXFP8 input ("[II] Support staged MXFP8 linear inputs", Behavior: empty_input
+ * allocates values and scale layouts; mm_quantized runs the GEMM on them). PARITY
+ * UNPINNED: the pages do not print this layout; it is the publicly described one:
+ * the scale matrix S [rows_total, g_total] (g_total = columns of the whole tensor / 32,
+ * a multiple of 4) is cut into tiles of 128 rows x 4 scale columns, tile (R, C) stored
+ * as 512 bytes at (R * g_total/4 + C) * 512, and inside a tile row r, column c at byte
+ * (r % 32) * 16 + (r / 32) * 4 + c. Rows past `rows` in the last tile row are not
+ * written (allocate bq_mx_tiled_scale_bytes and zero-fill if a consumer reads them).
+ *   x, rows, cols, ld_x, q_e4m3, ld_q   as bq_quant_mx (a slice of a wider tensor)
+ *   s_tiled    base of the whole tensor's tiled scale buffer (4-byte aligned)
+ *   g_total    scale columns of the whole tensor; g0 = the slice's first scale column
+ *              (column offset / 32), a multiple of 4; g0 + cols/32 <= g_total. */
+BQ_API bq_status bq_quant_mx_tiled(const void *x, int x_is_f16, int64_t rows, int64_t cols, int64_t ld_x,
+                            uint8_t *q_e4m3, int64_t ld_q, uint8_t *s_tiled, int64_t g_total,
+                            int64_t g0, cudaStream_t stream);
+
+/* Bytes of the tiled scale layout for rows x g_total scales (rows rounded up to 128);
+ * -1 if g_total is not a non-negative multiple of 4. */
+BQ_API int64_t bq_mx_tiled_scale_bytes(int64_t rows, int64_t g_total);
 
 /* The i8 mode's BF16 reduce-scatter fused with its INT8 all-gather payload
  * ("feat(pcie_dma): add block-INT8 wire modes for AG, ring, and A2A", Summary: i8 =

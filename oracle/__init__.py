@@ -27,6 +27,8 @@ Each function follows the pull-request pages on the wire codec:
   page, Summary.
 * ``quant_e4m3`` / ``dequant_e4m3``: the legacy E4M3 codec the block-INT8 page
   compares against (Summary and Why: one E4M3 byte per value, FP32 scale per 128).
+* ``mx_scales_to_tiled``: the tiled E8M0 layout block-scaled GEMMs read. PARITY
+  UNPINNED: the staged-input page names scale layouts for its GEMM but prints none.
 """
 from __future__ import annotations
 
@@ -79,6 +81,7 @@ def _load():
                 "bqo_reduce_quant_e4m3": [P, ctypes.c_int, I64, P, P, P],
                 "bqo_quant_e4m3": [P, I64, P, P],
                 "bqo_dequant_e4m3": [P, P, I64, P],
+                "bqo_mx_scales_to_tiled": [P, I64, I64, I64, P],
             }.items():
                 fn = getattr(lib, name)
                 fn.argtypes = args
@@ -91,6 +94,8 @@ def _load():
             lib.bqo_e4m3_decode.restype = ctypes.c_double
             lib.bqo_e8m0_scale.argtypes = [ctypes.c_float]
             lib.bqo_e8m0_scale.restype = ctypes.c_uint8
+            lib.bqo_mx_tiled_scale_offset.argtypes = [I64, I64, I64]
+            lib.bqo_mx_tiled_scale_offset.restype = I64
             lib.bqo_f16_to_float.argtypes = [ctypes.c_uint16]
             lib.bqo_f16_to_float.restype = ctypes.c_float
             lib.bqo_wire_bytes.argtypes = [I64]
@@ -330,6 +335,24 @@ def dequant_e4m3(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     out = np.empty(q.size, np.uint16)
     _check(_load().bqo_dequant_e4m3(_ptr(q), _ptr(s), q.size, _ptr(out)), "dequant_e4m3")
     return out
+
+
+def mx_tiled_scale_bytes(rows: int, g: int) -> int:
+    """Bytes of the tiled layout for [rows, g] scales (rows padded to 128, g % 4 == 0)."""
+    return ((rows + 127) // 128) * (g // 4) * 512
+
+
+def mx_scales_to_tiled(s: np.ndarray, fill: int = 0) -> np.ndarray:
+    """Row-major E8M0 [rows, g] -> the tiled layout (uint8, padding rows = fill)."""
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    rows, g = s.shape
+    out = np.full(mx_tiled_scale_bytes(rows, g), fill, np.uint8)
+    _check(_load().bqo_mx_scales_to_tiled(_ptr(s), rows, g, g, _ptr(out)), "mx_scales_to_tiled")
+    return out
+
+
+def mx_tiled_scale_offset(row: int, gcol: int, g: int) -> int:
+    return int(_load().bqo_mx_tiled_scale_offset(row, gcol, g))
 
 
 # ---------------------------------------------------------------- scalar helpers (for pins)

@@ -538,5 +538,37 @@ int bqo_reduce_quant_e4m3(const uint16_t *const *x_srcs, int W, int64_t n, uint8
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Tiled E8M0 scale layout for block-scaled GEMM operands.                   */
+/* PARITY UNPINNED: the staged-input page mentions scale layouts for the    */
+/* GEMM ("[II] Support staged MXFP8 linear inputs", Behavior: empty_input    */
+/* allocates MXFP8 values and scale layouts) but prints none. This is the   */
+/* tiled layout that Blackwell block-scaled matrix multiplies read, stated  */
+/* from its public description; nothing on the pages can confirm it.        */
+/*                                                                          */
+/* The scale matrix S [rows, g] (g = cols/32) is cut into tiles of 128 rows */
+/* by 4 scale columns; tile (R, C) holds rows 128R..128R+127 and columns    */
+/* 4C..4C+3 and occupies 512 bytes at offset (R * (g/4) + C) * 512. Inside  */
+/* the tile, row r and column c sit at byte                                  */
+/*     (r % 32) * 16 + (r / 32) * 4 + c      (r in 0..127, c in 0..3),       */
+/* i.e. four interleaved 32-row panels: each 16-byte line holds one row of  */
+/* every panel. Rows past `rows` in the last tile row are not written.       */
+/* ------------------------------------------------------------------------ */
+
+int64_t bqo_mx_tiled_scale_offset(int64_t row, int64_t gcol, int64_t g)
+{
+    int64_t R = row / 128, C = gcol / 4, r = row % 128, c = gcol % 4;
+    return (R * (g / 4) + C) * 512 + (r % 32) * 16 + (r / 32) * 4 + c;
+}
+
+/* Row-major E8M0 [rows][ld_s] -> tiled; g = cols/32 must be a multiple of 4. */
+int bqo_mx_scales_to_tiled(const uint8_t *s, int64_t rows, int64_t g, int64_t ld_s, uint8_t *tiled)
+{
+    if (rows < 0 || g < 0 || g % 4 || ld_s < g) return -1;
+    for (int64_t row = 0; row < rows; row++)
+        for (int64_t c = 0; c < g; c++) tiled[bqo_mx_tiled_scale_offset(row, c, g)] = s[row * ld_s + c];
+    return 0;
+}
+
 /* Wire size of an n-element tensor in either codec: 132 bytes per 128 values. */
 int64_t bqo_wire_bytes(int64_t n) { return n + 4 * (n / BQO_BLOCK); }

@@ -27,7 +27,8 @@ def test_header_declares_the_calls():
     names = declared_functions()
     for want in ("bq_quant_i8", "bq_dequant_i8", "bq_dequant_accum_i8", "bq_ring_hop_i8", "bq_quant_mx",
                  "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_quant_mx_f16", "bq_reduce_quant_i8",
-                 "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_wire_bytes", "bq_status_string",
+                 "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_quant_mx_tiled",
+                 "bq_mx_tiled_scale_bytes", "bq_wire_bytes", "bq_status_string",
                  "bq_abi_version", "bq_take_wait_timeouts", "bq_selftest_wait_timeout"):
         assert want in names
 
@@ -35,7 +36,7 @@ def test_header_declares_the_calls():
 def test_library_exports_every_declared_symbol(bq_lib):
     for name in declared_functions():
         assert hasattr(bq_lib, name), name
-    assert bq_lib.bq_abi_version() == 3
+    assert bq_lib.bq_abi_version() == 4
 
 
 def test_wire_bytes_and_status_strings(bq_lib):
@@ -202,6 +203,23 @@ def test_quant_mx_f16_rejections(bq_lib):
     assert f(A + 2, 4, 128, 128, A + 0x100000, 128, A + 0x200000, 4, None) == ALIGN
     assert f(A, 4, 128, 132, A + 0x100000, 128, A + 0x200000, 4, None) == ALIGN  # ld_x % 8
     assert f(A, 4, 128, 128, A + 512, 128, A + 0x200000, 4, None) == ALIAS
+
+
+def test_quant_mx_tiled_rejections(bq_lib):
+    f = bq_lib.bq_quant_mx_tiled
+    x, q, s = A, A + 0x1000000, A + 0x2000000
+    assert f(x, 0, 256, 100, 256, q, 256, s, 8, 0, None) == SHAPE      # cols % 128
+    assert f(x, 0, 256, 256, 256, q, 256, s, 6, 0, None) == SHAPE      # g_total % 4
+    assert f(x, 0, 256, 256, 256, q, 256, s, 8, 2, None) == SHAPE      # g0 % 4
+    assert f(x, 0, 256, 256, 256, q, 256, s, 8, 4, None) == SHAPE      # g0 + cols/32 > g_total
+    assert f(x, 0, 0, 256, 256, None, 256, None, 8, 0, None) == OK     # empty
+    assert f(None, 0, 256, 256, 256, q, 256, s, 8, 0, None) == NULL
+    assert f(x, 0, 256, 256, 256, q, 256, s + 2, 8, 0, None) == ALIGN
+    assert f(x, 1, 256, 256, 260, q, 256, s, 8, 0, None) == ALIGN     # ld_x % 8 != 0 (FP16 too)
+    assert f(x, 0, 256, 256, 256, q, 256, x + 512, 8, 0, None) == ALIAS
+    assert bq_lib.bq_mx_tiled_scale_bytes(256, 8) == 2 * 2 * 512
+    assert bq_lib.bq_mx_tiled_scale_bytes(300, 1344) == 3 * 336 * 512
+    assert bq_lib.bq_mx_tiled_scale_bytes(1, 6) == -1
 
 
 def test_mx_rejections(bq_lib):

@@ -237,3 +237,29 @@ def test_mx_f16_every_value_and_ragged_rows():
     qr2, sr2 = oracle.quant_mx(y.view(np.uint16), fmt="f16")
     assert_same(q2, qr2, "codes")
     assert_same(s2, sr2, "scales")
+
+
+# ------------------------------------------------------------------ tiled scale layout (parity unpinned vs the pages)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_mx_tiled_scales_staged_slices(dtype):
+    # six staged slices of 300 rows (a ragged last tile row) into one tiled scale buffer;
+    # codes equal the row-major call's, scales equal the oracle's scales placed by the
+    # oracle's tiled layout, and the padding rows of the last tile row stay untouched
+    slices = inputs.mx_slices_4096(rows=300, n_slices=6, dtype=dtype)
+    rows, cols = slices[0].shape
+    C = 6 * cols
+    g_total = C // 32
+    q, s_rm = codec.empty_mx(rows, C)
+    q_t = torch.empty_like(q)
+    tiled = torch.full((codec.mx_tiled_scale_bytes(rows, g_total),), 0xA5, dtype=torch.uint8, device="cuda")
+    for i, x in enumerate(slices):
+        c0 = i * cols
+        codec.quant_mx(x, q[:, c0:c0 + cols], s_rm[:, c0 // 32:(c0 + cols) // 32])
+        codec.quant_mx_tiled(x, q_t[:, c0:c0 + cols], tiled, g_total, c0 // 32)
+    assert torch.equal(q, q_t)
+    fmt = "f16" if dtype == torch.float16 else "bf16"
+    qr, sr = oracle.quant_mx((torch.cat(slices, dim=1).contiguous().view(torch.int16).cpu().numpy().view(np.uint16)),
+                             fmt=fmt)
+    assert_same(q, qr, "codes")
+    want = oracle.mx_scales_to_tiled(sr, fill=0xA5)
+    assert_same(tiled, want, "tiled scales")

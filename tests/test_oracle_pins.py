@@ -792,6 +792,29 @@ def test_mx_f16_staged_slices_equal_concatenated():
     assert np.array_equal(q_buf, q) and np.array_equal(s_buf, s)
 
 
+# ------------------------------------------------------------------ tiled scale layout
+def test_mx_tiled_scale_layout_is_a_tile_wise_bijection():
+    # PARITY UNPINNED against the pages (they print no GEMM scale layout); these checks
+    # only confirm that the oracle's layout is the stated one: every scale lands in its
+    # own byte, each 128 x 4 tile is one contiguous 512-byte run in row-tile-major order,
+    # and inside a tile each 16-byte line holds rows r, r+32, r+64, r+96.
+    rows, g = 256, 12
+    seen = {}
+    for r in range(rows):
+        for c in range(g):
+            off = oracle.mx_tiled_scale_offset(r, c, g)
+            assert off not in seen
+            seen[off] = (r, c)
+            tile = off // 512
+            assert tile == (r // 128) * (g // 4) + c // 4
+            within = off % 512
+            assert within // 16 == r % 32 and (within % 16) // 4 == (r % 128) // 32 and within % 4 == c % 4
+    assert sorted(seen) == list(range(oracle.mx_tiled_scale_bytes(rows, g)))
+    s = np.arange(rows * g, dtype=np.uint32).astype(np.uint8).reshape(rows, g)
+    t = oracle.mx_scales_to_tiled(s)
+    assert all(t[off] == s[r, c] for off, (r, c) in seen.items())
+
+
 # ------------------------------------------------------------------ staged == concatenated
 def test_staged_slices_equal_concatenated():
     # "[II] Support staged MXFP8 linear inputs": quantizing 128-column-aligned slices
