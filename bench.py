@@ -390,15 +390,41 @@ def cpu_inputs(rows: int, slice_rows: int):
 
 
 # ---------------------------------------------------------------- widened rows
+def graph_ms(fn, reps: int) -> float:
+    """Average device time of one call of fn: `reps` calls captured into one CUDA graph
+    (after 3 eager warm-ups) and the graph timed by CUDA events around one replay, so
+    the host's launch overhead is not in the number (short launches would otherwise
+    wait for the host)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del g
+    return ms
+
+
 def time_next_rows(pipe, args, peak):
     """Per-launch duration of the kernels beyond the step, on the prefill buffers:
     dequant_accum_mx (W=4) and ring_hop_mx on flat MX wires quantized from them,
     reduce_quant_i8 / reduce_quant_e4m3 (W=4: the all-gather modes' fused reduce),
     quant_e4m3 / dequant_e4m3 (legacy codec), and quant_mx on FP16 slices of the staged
-    workload (rotating over six slices). CUDA events around `next_reps` back-to-back
-    launches of each kernel on the launching stream, after 3 warm-up launches; every
-    launch (or, for the slices, every six consecutive launches) moves more than the
-    129 MB L2 holds."""
+    workload (rotating over six slices). Each kernel: `next_reps` back-to-back launches
+    replayed as one CUDA graph (graph_ms); every launch (or, for the slices, every six
+    consecutive launches) moves more than the 129 MB L2 holds."""
     from block_quantized_wire_gb300 import inputs
     c = pipe.codec
     n = pipe.n
@@ -433,21 +459,69 @@ def time_next_rows(pipe, args, peak):
     }
     out = {}
     for name, (fn, nv) in runs.items():
-        for _ in range(3):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record()
-        for _ in range(args.next_reps):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        avg_ms = e0.elapsed_time(e1) / args.next_reps
+        avg_ms = graph_ms(fn, args.next_reps)
         nbytes = kernel_bytes(name, nv)
         gbs = nbytes / (avg_ms * 1e-3) / 1e9
         out[name] = {"launches": args.next_reps, "avg_us": round(avg_ms * 1e3, 2), "bytes_per_launch": nbytes,
                      "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
     del wires, ew, iw, f16
+    return out
+
+
+# ---------------------------------------------------------------- the smaller configs
+def time_configs(args, peak):
+    """Per-kernel launch duration on the four smaller workloads (512, 3072, 3072 x W=4
+    and 16384 x W=4 rows of 7168), inputs drawn on the device with the workloads' seeds
+    and structure, each kernel timed as `next_reps` launches replayed from one CUDA
+    graph (graph_ms). A launch whose bytes fit in the 129 MB L2 is labelled L2-warm:
+    repeated launches read it from L2."""
+    from block_quantized_wire_gb300 import codec, inputs
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L2 = 129 * 10 ** 6
+    out = {}
+
+    def timed(fn, name, n, cfg):
+        ms = graph_ms(fn, args.next_reps)
+        nbytes = kernel_bytes(name, n) if name in ("quant_i8", "dequant_i8", "quant_mx", "dequant_mx",
+                                                   "dequant_accum_i8", "ring_hop_i8") else None
+        if name == "dequant_accum_i8+bf16":
+            nbytes = kernel_bytes("dequant_accum_i8", n) + 2 * n
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out.setdefault(cfg, {})[name] = {"avg_us": round(ms * 1e3, 2), "bytes_per_launch": nbytes,
+                                         "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                                         "l2": "warm" if nbytes < L2 else "cold"}
+
+    x1 = inputs.roundtrip_512(device=dev)
+    _, q1, s1 = codec.empty_wire_i8(x1.numel(), dev)
+    o1 = torch.empty_like(x1)
+    timed(lambda: codec.quant_i8(x1.view(-1), q1, s1), "quant_i8", x1.numel(), "roundtrip_512")
+    timed(lambda: codec.dequant_i8(q1, s1, o1.view(-1)), "dequant_i8", x1.numel(), "roundtrip_512")
+    x2 = inputs.mixed_3072(device=dev)
+    n2 = x2.numel()
+    _, q2, s2 = codec.empty_wire_i8(n2, dev)
+    o2 = torch.empty_like(x2)
+    mq, ms_ = codec.empty_mx(*x2.shape, dev)
+    timed(lambda: codec.quant_i8(x2.view(-1), q2, s2), "quant_i8", n2, "mixed_3072")
+    timed(lambda: codec.dequant_i8(q2, s2, o2.view(-1)), "dequant_i8", n2, "mixed_3072")
+    timed(lambda: codec.quant_mx(x2, mq, ms_), "quant_mx", n2, "mixed_3072")
+    timed(lambda: codec.dequant_mx(mq, ms_, o2), "dequant_mx", n2, "mixed_3072")
+    xs3 = inputs.a2a_3072(device=dev)
+    w3 = [codec.empty_wire_i8(n2, dev) for _ in range(W_SRC + 1)]
+    for w in range(W_SRC):
+        codec.quant_i8(xs3[w].view(-1), w3[w][1], w3[w][2])
+    src_q, src_s = [w3[w][1] for w in range(W_SRC)], [w3[w][2] for w in range(W_SRC)]
+    timed(lambda: codec.dequant_accum_i8(src_q, src_s, w3[W_SRC][1], w3[W_SRC][2], None), "dequant_accum_i8", n2,
+          "a2a_3072")
+    timed(lambda: codec.dequant_accum_i8(src_q, src_s, w3[W_SRC][1], w3[W_SRC][2], o2.view(-1)),
+          "dequant_accum_i8+bf16", n2, "a2a_3072")
+    del xs3, w3
+    xs4 = inputs.ring_16384(device=dev)
+    n4 = xs4[0].numel()
+    w4 = [codec.empty_wire_i8(n4, dev) for _ in range(2)]
+    codec.quant_i8(xs4[0].view(-1), w4[0][1], w4[0][2])
+    timed(lambda: codec.ring_hop_i8(w4[0][1], w4[0][2], xs4[1].view(-1), w4[1][1], w4[1][2], None), "ring_hop_i8",
+          n4, "ring_16384 (one hop step over the 4 shards)")
+    del xs4, w4
     return out
 
 
@@ -531,6 +605,7 @@ def run_bq(args, rank, world, local):
     # The MXFP8 wire reductions (mx_a2a accumulate, mx_ring hop) on the same prefill
     # buffers: rows that widen the hot path, timed apart from the step.
     next_rows = None if args.no_next else time_next_rows(pipe, args, peak)
+    configs = None if args.no_next else time_configs(args, peak)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -577,7 +652,7 @@ def run_bq(args, rank, world, local):
                    "step_bytes": step_bytes, "launches_per_step": nl,
                    "l2": "no flush: step working set ~12.5 GB >> 129 MB L2",
                    "parallelism": f"replicas x{world} (no collective)"},
-        "roofline": roofline, "kernels": kernels, "next_rows": next_rows, "clocks": clocks,
+        "roofline": roofline, "kernels": kernels, "next_rows": next_rows, "configs": configs, "clocks": clocks,
         "e2e": e2e, "gpu_launches": nl * args.steps, "cpu_baseline": cpu,
         "device": torch.cuda.get_device_name(dev),
     }
@@ -629,7 +704,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-next", action="store_true", help="skip timing the MX wire reductions")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip timing the kernels beyond the step and the smaller configs")
     ap.add_argument("--next-reps", type=int, default=24)
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--cpu-slice-rows", type=int, default=256)
