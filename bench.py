@@ -132,12 +132,20 @@ def load_traffic():
 
 
 def kernel_sources_sha() -> str:
+    """Hash of the kernel sources' code: every file of csrc with comments removed and
+    whitespace collapsed, so that a comment edit does not invalidate the recorded ncu
+    counters while any code change does."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_wire_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(f.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 

@@ -1,11 +1,14 @@
-// Warp-chunk drivers and the two wire reductions shared by both codecs.
+// Warp-chunk drivers and the codec operations shared by the wire formats: quantize,
+// materialize, the all-to-all accumulate, the ring hop, and the all-gather modes'
+// reduce + quantize.
 //
-// Both wires carry, per 128-value block, 128 payload bytes and 4 scale bytes: one
+// Every wire carries, per 128-value block, 128 payload bytes and 4 scale bytes: one
 // FP32 scale for block INT8 ("feat(pcie_dma): add block-INT8 wire modes for AG,
-// ring, and A2A", Summary) and four E8M0 bytes, one per 32 values, for MXFP8
-// ("feat(pcie_dma): add INT8 and MXFP8 wire modes", Summary). A flat wire of n values
-// is the payload [n] followed by the scale words [n/128], so the same loads serve
-// both; a codec policy supplies what differs:
+// ring, and A2A", Summary) and for the legacy E4M3 codec it compares against, and four
+// E8M0 bytes, one per 32 values, for MXFP8 ("feat(pcie_dma): add INT8 and MXFP8 wire
+// modes", Summary). A flat wire of n values is the payload [n] followed by the scale
+// words [n/128], so the same loads serve all three; a codec policy supplies what
+// differs:
 //
 //   struct Codec {
 //     using Q = payload element type;  using S = 4-byte scale word type;

@@ -1,8 +1,9 @@
 /*
  * bq.h — C ABI of libbq.so, the block-quantized wire codec for GB300 (sm_103a).
  *
- * The codec compresses BF16 all-reduce payloads into two wire formats, each 132
- * bytes per 128 values:
+ * The codec compresses BF16 all-reduce payloads into wire formats of 132 bytes per
+ * 128 values: the two of the pages' compressed modes below, and the legacy E4M3 codec
+ * (one E4M3 byte per value and one FP32 scale per 128 values) they replace:
  *
  *   block INT8   128 signed payload bytes + one FP32 scale = amax/127 per block of
  *                128 consecutive values ("feat(pcie_dma): add block-INT8 wire modes
