@@ -597,6 +597,22 @@ def run_bq(args, rank, world, local):
         kernels[name] = {"launches_per_step": d["launches"] // args.steps, "avg_us": round(avg_ms * 1e3, 2),
                          "bytes_per_launch": d["bytes"], "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                          "share": round(d["ms"] / ms_instr, 4)}
+    # the same kernels timed without the gaps that an event after every launch leaves:
+    # each one's launches of a step, repeated, replayed from one CUDA graph
+    if not args.no_next:
+        by_name = {}
+        for name, fn, nbytes in pipe.launches:
+            by_name.setdefault(name, []).append((fn, nbytes))
+        for name, fns in by_name.items():
+            turn = [0]
+
+            def rotate(fns=fns, turn=turn):
+                fns[turn[0] % len(fns)][0]()
+                turn[0] += 1
+            gms = graph_ms(rotate, max(args.next_reps, len(fns) * 4))
+            gbs_g = fns[0][1] / (gms * 1e-3) / 1e9
+            kernels[name].update({"graph_avg_us": round(gms * 1e3, 2), "graph_GB/s": round(gbs_g, 1),
+                                  "graph_frac": round(gbs_g / peak, 4)})
     dominant = max(per, key=lambda k: per[k]["ms"])
     dk = kernels[dominant]
     traffic = None
