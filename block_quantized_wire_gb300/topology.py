@@ -170,3 +170,33 @@ def i8_ag(xs, stream=None):
 def e4m3_ag(xs, stream=None):
     """The E4M3 all-gather mode with the legacy E4M3 codec."""
     return _allgather(codec.reduce_quant_e4m3, codec.empty_wire_e4m3, codec.dequant_e4m3, xs, stream)
+
+
+# Mode selection by name ("feat(pcie_dma): add INT8 and MXFP8 wire modes", Modes:
+# names are matched after trimming surrounding whitespace and ignoring case; an empty
+# name keeps the uncompressed BF16 path; any other unknown name is an error rather than
+# a silent fallback).
+MODES = {
+    "i8": i8_roundtrip,     # per-shard quantize -> materialize of the INT8 all-gather
+    "i8_ring": i8_ring,
+    "i8_a2a": i8_a2a,
+    "i8_ag": i8_ag,         # BF16 reduce-scatter fused with the INT8 all-gather payload
+    "mx": mx_roundtrip,
+    "mx_ring": mx_ring,
+    "mx_a2a": mx_a2a,
+    "e4m3_ag": e4m3_ag,
+}
+
+
+def select_mode(name):
+    """The topology function for a wire-mode name, or None for the BF16 path (empty or
+    whitespace-only name). Raises ValueError for any other unknown name."""
+    if name is None:
+        return None
+    key = str(name).strip().lower()
+    if not key:
+        return None
+    try:
+        return MODES[key]
+    except KeyError:
+        raise ValueError(f"unknown wire mode {name!r}; expected one of {sorted(MODES)} or empty for BF16") from None
