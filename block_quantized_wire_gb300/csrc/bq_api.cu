@@ -50,7 +50,7 @@ namespace bqk {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxKernels = 64;
+constexpr int kMaxKernels = 1024;  // (kernel, dynamic smem, device) entries
 std::atomic<int> g_sms[kMaxDevices];
 struct OccEntry {
     const void *kernel;
