@@ -534,6 +534,23 @@ def time_configs(args, peak):
 
 
 # ---------------------------------------------------------------- arms
+def workload_config(args, world: int) -> dict:
+    """The `config` of both arms' JSON lines: the prefill step's workload."""
+    return {"workload": f"prefill pipeline: 4 x BF16 {args.rows}x{HIDDEN} quant_i8 -> dequant_accum_i8 (W=4) "
+                        f"-> dequant_i8, ring_hop_i8; 6 x BF16 {args.slice_rows}x{HIDDEN} quant_mx staged into "
+                        f"{args.slice_rows}x{HIDDEN * N_SLICES}, dequant_mx",
+            "step_bytes": step_bytes_of(args.rows, args.slice_rows), "launches_per_step": 4 + 3 + N_SLICES + 1,
+            "l2": "no flush: step working set ~12.5 GB >> 129 MB L2",
+            "parallelism": f"replicas x{world} (no collective)"}
+
+
+def step_bytes_of(rows: int, slice_rows: int) -> int:
+    n, ns = rows * HIDDEN, slice_rows * HIDDEN
+    return (W_SRC * kernel_bytes("quant_i8", n) + kernel_bytes("dequant_accum_i8", n) + kernel_bytes("dequant_i8", n)
+            + kernel_bytes("ring_hop_i8", n) + N_SLICES * kernel_bytes("quant_mx", ns)
+            + kernel_bytes("dequant_mx", ns * N_SLICES))
+
+
 def run_bq(args, rank, world, local):
     from block_quantized_wire_gb300 import build as bq_build
     bq_build.build_library()
@@ -670,12 +687,7 @@ def run_bq(args, rank, world, local):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"prefill pipeline: 4 x BF16 {args.rows}x{HIDDEN} quant_i8 -> dequant_accum_i8 (W=4) "
-                               f"-> dequant_i8, ring_hop_i8; 6 x BF16 {args.slice_rows}x{HIDDEN} quant_mx staged into "
-                               f"{args.slice_rows}x{HIDDEN * N_SLICES}, dequant_mx",
-                   "step_bytes": step_bytes, "launches_per_step": nl,
-                   "l2": "no flush: step working set ~12.5 GB >> 129 MB L2",
-                   "parallelism": f"replicas x{world} (no collective)"},
+        "config": workload_config(args, world),
         "roofline": roofline, "kernels": kernels, "next_rows": next_rows, "configs": configs, "clocks": clocks,
         "e2e": e2e, "gpu_launches": nl * args.steps, "cpu_baseline": cpu,
         "device": torch.cuda.get_device_name(dev),
@@ -710,7 +722,7 @@ def run_reference(args, rank, world, local):
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-        "config": {"workload": "prefill pipeline (sampled rows), same operations as the bq arm"},
+        "config": workload_config(args, world),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "kind": "oracle", "cores": cores, "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -31,6 +31,7 @@ def test_algorithmic_bytes_per_launch():
     assert bench.kernel_bytes("quant_mx_f16", 4096 * 7168) == 88997888
     step = (4 * 1423966208 + 2422210560 + 1423966208 + 1908408320 + 6 * 88997888 + 533987328)
     assert step == 12518424576
+    assert bench.step_bytes_of(65536, 4096) == step
 
 
 def _free_port():
@@ -107,6 +108,9 @@ def test_reference_arm_on_cpu():
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    # the same config as the codec arm's line for this workload
+    assert d["config"]["workload"].startswith("prefill pipeline: 4 x BF16 65536x7168")
+    assert d["config"]["step_bytes"] == 12518424576 and d["config"]["launches_per_step"] == 14
 
 
 def test_reference_arm_under_torchrun_world2():
