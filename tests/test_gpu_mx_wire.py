@@ -313,3 +313,49 @@ def test_mx_reductions_graph_replay_is_bit_identical():
     torch.cuda.synchronize()
     for a, b in zip(eager, [w[0] for w in wires] + [owner]):
         assert torch.equal(a, b)
+
+
+def test_mx_ring_chain_full_size_sampled():
+    # the 16384-row ring chain (4 shards of 4096 rows, 1 quantize + 3 hops each) at full
+    # size on the GPU; every element's chain is independent, so the oracle recomputes
+    # the chain on 2048 sampled 128-value blocks of every shard
+    xs = [x.cuda() for x in inputs.ring_16384()]
+    W = len(xs)
+    outs, finals, owners = topology.mx_ring(xs)
+    torch.cuda.synchronize()
+    nblk_shard = xs[0].numel() // W // 128
+    rng = np.random.default_rng(61)
+    for c in range(W):
+        blk = np.sort(rng.choice(nblk_shard, 2048, replace=False))
+        blk[-1] = nblk_shard - 1
+        idx = torch.from_numpy(blk).cuda()
+        shard = [x.reshape(W, -1)[c].reshape(-1, 128)[idx] for x in xs]
+        chain = topology.ring_order(c, W)
+        q, s = oracle.quant_mx_flat(bits(shard[chain[0]]))
+        for rank in chain[1:]:
+            q, s, _ = oracle.ring_hop_mx(q, s, bits(shard[rank]))
+        assert_same(finals[c][0].reshape(-1, 128)[idx], q, f"shard {c} codes")
+        assert_same(finals[c][1].reshape(-1, 4)[idx], s, f"shard {c} scales")
+        assert_same(owners[c].reshape(-1, 128)[idx], oracle.dequant_mx_flat(q, s), f"shard {c} owner")
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_mx_modes_error_vs_unquantized_sum():
+    # each MX requantization moves a value by at most half an E4M3 spacing at its
+    # scaled magnitude, relative 2^-4 of the value for normal codes plus 2^-10 * 2^(e-127)
+    # absolutely; the a2a owner output stays within the sum of those bounds of the exact
+    # sum of the BF16 inputs (plus half a BF16 ulp of the output)
+    xs = [x.cuda() for x in inputs.a2a_3072(rows=256)]
+    q_out, s_out, owner, srcs = topology.mx_a2a(xs)
+    exact = sum(x.double() for x in xs).reshape(-1, 32)
+    def group_bound(s_bytes, vals):
+        scale = torch.exp2(s_bytes.double() - 127)[:, None]
+        return vals.abs() * 2.0 ** -4 + scale * 2.0 ** -10
+    bound = sum(group_bound(s.reshape(-1), x.double().reshape(-1, 32)) for (_, s), x in zip(srcs, xs))
+    # the requantization's term is relative to the binary32 sum, which exceeds the
+    # owner output by at most 1 / (1 - 2^-4) and half a BF16 ulp: 1.1 covers both
+    bound = bound + group_bound(s_out.reshape(-1), owner.double().reshape(-1, 32) * 1.1)
+    bound = bound + owner.double().reshape(-1, 32).abs() * 2.0 ** -8 + 1e-30
+    err = (owner.double().reshape(-1, 32) - exact).abs()
+    assert bool((err <= bound * (1 + 2.0 ** -10)).all())

@@ -105,6 +105,7 @@ def test_bounded_waits_do_not_run_out_and_can_be_observed():
     codec.take_wait_timeouts()  # clear whatever earlier tests left
     xs = [x.cuda() for x in inputs.a2a_3072(rows=3072)]
     topology.i8_a2a(xs)
+    topology.mx_ring(xs)  # the MX hop stages its inputs too (its own counter)
     torch.cuda.synchronize()
     assert codec.take_wait_timeouts() == 0
     # a wait that nothing completes gives up after its limit and is counted; the
