@@ -28,8 +28,20 @@ def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
+        cur = torch.cuda.current_device()
+        if stream.device.index != cur:
+            raise ValueError(f"stream belongs to {stream.device}, but the current CUDA device is cuda:{cur}")
         return stream.cuda_stream
     return int(stream)
+
+
+def _on_current_device(t: torch.Tensor, name: str) -> None:
+    """The library launches on the current device, so every tensor must live there (a
+    pointer into another device's memory would be dereferenced by the wrong GPU)."""
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name}: tensor is on {t.device}, but the current CUDA device is cuda:{cur} "
+                         f"(run the call under torch.cuda.device({t.device.index}))")
 
 
 def _flat(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
@@ -37,6 +49,7 @@ def _flat(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name}: expected a CUDA tensor")
+    _on_current_device(t, name)
     if not t.is_contiguous():
         raise ValueError(f"{name}: expected a contiguous tensor")
     return t.data_ptr()
@@ -48,6 +61,7 @@ def _rows(t: torch.Tensor, dtype: torch.dtype, name: str):
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name}: expected a CUDA tensor")
+    _on_current_device(t, name)
     if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
         raise ValueError(f"{name}: expected a 2-D row-major view with unit column stride")
     ld = t.stride(0) if t.shape[0] > 1 else t.shape[1]

@@ -253,3 +253,44 @@ def test_binding_without_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(ImportError):
         _lib.load()
+
+
+class _FakeCudaTensor:
+    """Just enough of a CUDA tensor for the binding's argument checks (no memory)."""
+
+    def __init__(self, dtype, n, device_index):
+        import torch
+        self.dtype = dtype
+        self.is_cuda = True
+        self.device = torch.device("cuda", device_index)
+        self._n = n
+
+    def is_contiguous(self):
+        return True
+
+    def numel(self):
+        return self._n
+
+    def data_ptr(self):
+        return A
+
+
+def test_binding_rejects_tensors_on_another_device(monkeypatch):
+    # launches go to the current device, so a tensor on another device is refused
+    # before the library is called
+    import torch
+    from block_quantized_wire_gb300 import codec
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    called = []
+    monkeypatch.setattr(codec, "check", lambda *a: called.append(a))
+    n = 1024
+    x = _FakeCudaTensor(torch.bfloat16, n, 1)
+    q = _FakeCudaTensor(torch.int8, n, 0)
+    s = _FakeCudaTensor(torch.float32, n // 128, 0)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        codec.quant_i8(x, q, s, stream=0)
+    x0 = _FakeCudaTensor(torch.bfloat16, n, 0)
+    q1 = _FakeCudaTensor(torch.int8, n, 1)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        codec.quant_i8(x0, q1, s, stream=0)
+    assert not called
