@@ -8,6 +8,7 @@ results are fixed by their explicit ``__f*_rn`` operations alone.
 from __future__ import annotations
 
 import concurrent.futures
+import fcntl
 import os
 import shutil
 import subprocess
@@ -50,10 +51,25 @@ def up_to_date() -> bool:
 
 
 def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libbq.so if any source is newer than it; returns its path."""
+    """Compile and link libbq.so if any source is newer than it; returns its path.
+
+    Concurrent callers (one process per GPU under torchrun) are serialized by a file
+    lock: the first builds, the others find the library up to date. The library is
+    replaced atomically, so a process that already loaded it is unaffected."""
     if not force and up_to_date():
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)
+    with open(os.path.join(OBJDIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIB
+            return _build_locked(verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool, extra_flags) -> str:
     cc = nvcc()
 
     def compile_one(src):
