@@ -603,15 +603,18 @@ def run_bq(args, rank, world, local):
         for i, (name, _, nbytes) in enumerate(pipe.launches):
             t = prev.elapsed_time(events[k][i])
             prev = events[k][i]
-            d = per.setdefault(name, {"ms": 0.0, "launches": 0, "bytes": nbytes})
+            d = per.setdefault(name, {"ms": 0.0, "launches": 0, "bytes": nbytes, "samples": []})
             d["ms"] += t
             d["launches"] += 1
+            d["samples"].append(t)
     peak, peak_kind = load_peaks()
     kernels = {}
     for name, d in per.items():
         avg_ms = d["ms"] / d["launches"]
         gbs = d["bytes"] / (avg_ms * 1e-3) / 1e9
-        kernels[name] = {"launches_per_step": d["launches"] // args.steps, "avg_us": round(avg_ms * 1e3, 2),
+        q = sorted(d["samples"])
+        pct = {f"p{p}_us": round(q[min(len(q) - 1, int(p / 100 * len(q)))] * 1e3, 2) for p in (10, 50, 90)}
+        kernels[name] = {"launches_per_step": d["launches"] // args.steps, "avg_us": round(avg_ms * 1e3, 2), **pct,
                          "bytes_per_launch": d["bytes"], "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                          "share": round(d["ms"] / ms_instr, 4)}
     # the same kernels timed without the gaps that an event after every launch leaves:
