@@ -106,7 +106,8 @@ def test_reference_arm_on_cpu():
     d = lines[0]
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is True
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    from oracle import shards
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == shards.host_cores()
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     # the same config as the codec arm's line for this workload
     assert d["config"]["workload"].startswith("prefill pipeline: 4 x BF16 65536x7168")
