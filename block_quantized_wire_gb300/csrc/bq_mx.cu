@@ -70,35 +70,59 @@ __device__ __forceinline__ int64_t scale_offset(const ChunkPos &p, int k, int64_
     return ((r >> 7) * ld_s + c0 + cb) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
 }
 
-// One warp chunk = 4 segments = 8 blocks = 32 groups of 32 values. After the group
-// amaxes are reduced (4 lanes per group), lane L gathers the amax of the chunk's group
-// L (group order = scale-byte order within the chunk: block-major, 4 groups per
-// block) and computes that group's E8M0 byte and multiplier 2^(127-e) once; each lane
-// then fetches its own group's multiplier per segment, and lanes 4b (b = 0..7) store
-// block b's four scale bytes as one 32-bit word.
-template <bool kF16, bool kTiled, bool kTail, bool kOneRow>
-__device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
-                                               int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
-                                               uint8_t *__restrict__ s, int64_t ld_s, int64_t c0, int64_t b0,
-                                               ChunkPos pos, int lane)
+// One warp chunk = 4 segments = 8 blocks = 32 groups of 32 values. A lane loads 16
+// bytes (8 values) of block 2j + half for each segment j.
+template <bool kTail, bool kOneRow>
+__device__ __forceinline__ void quant_mx_load(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk,
+                                              int64_t b0, ChunkPos pos, int lane, uint4 (&raw)[kSegs])
 {
-    constexpr int SEGS = kSegs;
     const int half = lane >> 4, hl = lane & 15;
-    uint4 raw[SEGS];
 #pragma unroll
-    for (int j = 0; j < SEGS; j++) {
+    for (int j = 0; j < kSegs; j++) {
         const int64_t ox = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_x, 128);
         raw[j] = (!kTail || b0 + 2 * j + half < nblk) ? ld_stream_v4(x + ox + hl * 8) : make_uint4(0, 0, 0, 0);
     }
-    float2 v[SEGS][4];
+}
+
+template <bool kTail>
+__device__ __forceinline__ void quant_mx_load_any(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
+                                                  int64_t nblk, int64_t b0, ChunkPos pos, int lane,
+                                                  uint4 (&raw)[kSegs])
+{
+    if (pos.cb0 + kChunkBlocks <= bpr)
+        quant_mx_load<kTail, true>(x, ld_x, bpr, nblk, b0, pos, lane, raw);
+    else
+        quant_mx_load<kTail, false>(x, ld_x, bpr, nblk, b0, pos, lane, raw);
+}
+
+template <bool kF16>
+__device__ __forceinline__ void widen8(const uint4 &raw, float2 (&v)[4])
+{
+    if (kF16)
+        f16x8_to_f32(raw, v);
+    else
+        bf16x8_to_f32(raw, v);
+}
+
+// Quantize a loaded chunk. After the group amaxes are reduced (4 lanes per group), lane
+// L gathers the amax of the chunk's group L (group order = scale-byte order within the
+// chunk: block-major, 4 groups per block) and computes that group's E8M0 byte and
+// multiplier 2^(127-e) once; each lane then fetches its own group's multiplier per
+// segment, and lanes 4b (b = 0..7) store block b's four scale bytes as one 32-bit word.
+// The values are widened from the raw registers twice (for the amax, then for the
+// codes) rather than kept as 32 floats: 64 registers instead of 80.
+template <bool kF16, bool kTiled, bool kTail, bool kOneRow>
+__device__ __forceinline__ void quant_mx_compute(const uint4 (&raw)[kSegs], int64_t bpr, int64_t nblk,
+                                                 uint8_t *__restrict__ q, int64_t ld_q, uint8_t *__restrict__ s,
+                                                 int64_t ld_s, int64_t c0, int64_t b0, ChunkPos pos, int lane)
+{
+    const int half = lane >> 4, hl = lane & 15;
     float gmax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < SEGS; j++) {
-        if (kF16)
-            f16x8_to_f32(raw[j], v[j]);
-        else
-            bf16x8_to_f32(raw[j], v[j]);
-        float m = amax8(v[j]);
+    for (int j = 0; j < kSegs; j++) {
+        float2 v[4];
+        widen8<kF16>(raw[j], v);
+        float m = amax8(v);
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
         const float g = __shfl_sync(kFull, m, (lane & 7) << 2);
@@ -107,11 +131,12 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
     const uint32_t e = mx_scale_byte(gmax);
     const float p = exp2i(127 - static_cast<int>(e));
 #pragma unroll
-    for (int j = 0; j < SEGS; j++) {
+    for (int j = 0; j < kSegs; j++) {
         const float2 pj = splat(__shfl_sync(kFull, p, 8 * j + (lane >> 2)));
-        float2 y[4];
+        float2 v[4], y[4];
+        widen8<kF16>(raw[j], v);
 #pragma unroll
-        for (int i = 0; i < 4; i++) y[i] = mul2(v[j][i], pj);  // exact: a power-of-two scaling
+        for (int i = 0; i < 4; i++) y[i] = mul2(v[i], pj);  // exact: a power-of-two scaling
         if (!kTail || b0 + 2 * j + half < nblk) {
             const int64_t oq = block_offset<kOneRow>(pos, 2 * j + half, bpr, ld_q, 128);
             st_v2(q + oq + hl * 8, f32x8_to_e4m3x8(y));
@@ -125,15 +150,14 @@ __device__ __forceinline__ void quant_mx_chunk(const uint16_t *__restrict__ x, i
 }
 
 template <bool kF16, bool kTiled, bool kTail>
-__device__ __forceinline__ void quant_mx_chunk_any(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr,
-                                                   int64_t nblk, uint8_t *__restrict__ q, int64_t ld_q,
-                                                   uint8_t *__restrict__ s, int64_t ld_s, int64_t c0, int64_t b0,
-                                                   ChunkPos pos, int lane)
+__device__ __forceinline__ void quant_mx_compute_any(const uint4 (&raw)[kSegs], int64_t bpr, int64_t nblk,
+                                                     uint8_t *__restrict__ q, int64_t ld_q, uint8_t *__restrict__ s,
+                                                     int64_t ld_s, int64_t c0, int64_t b0, ChunkPos pos, int lane)
 {
     if (pos.cb0 + kChunkBlocks <= bpr)
-        quant_mx_chunk<kF16, kTiled, kTail, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, b0, pos, lane);
+        quant_mx_compute<kF16, kTiled, kTail, true>(raw, bpr, nblk, q, ld_q, s, ld_s, c0, b0, pos, lane);
     else
-        quant_mx_chunk<kF16, kTiled, kTail, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, b0, pos, lane);
+        quant_mx_compute<kF16, kTiled, kTail, false>(raw, bpr, nblk, q, ld_q, s, ld_s, c0, b0, pos, lane);
 }
 
 // Grid-stride walk over chunks with the chunk's (row, column block) advanced
@@ -169,8 +193,11 @@ struct ChunkWalkT {
 };
 using ChunkWalk = ChunkWalkT<kChunkBlocks>;
 
+// 4 resident CTAs per SM (64 registers, no spills): 16.4 us per 4096x7168 slice on
+// GB300 against 16.8 us at 3 CTAs per SM. Issuing the next chunk's loads before
+// quantizing the current one (80 registers, 3 CTAs per SM) measured the same, 16.5 us.
 #ifndef BQ_QUANT_MX_MIN_CTAS
-#define BQ_QUANT_MX_MIN_CTAS 3
+#define BQ_QUANT_MX_MIN_CTAS 4
 #endif
 
 // kF16: the input is FP16 instead of BF16. kTiled: scales go to the tiled GEMM layout
@@ -184,10 +211,16 @@ quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
     ChunkWalk w(bpr);
-    for (; w.c < nfull; w.next())
-        quant_mx_chunk_any<kF16, kTiled, false>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
-    if (w.c == nfull && nblk % kChunkBlocks)
-        quant_mx_chunk_any<kF16, kTiled, true>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
+    for (; w.c < nfull; w.next()) {
+        uint4 raw[kSegs];
+        quant_mx_load_any<false>(x, ld_x, bpr, nblk, w.b0, w.pos, lane, raw);
+        quant_mx_compute_any<kF16, kTiled, false>(raw, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
+    }
+    if (w.c == nfull && nblk % kChunkBlocks) {
+        uint4 raw[kSegs];
+        quant_mx_load_any<true>(x, ld_x, bpr, nblk, w.b0, w.pos, lane, raw);
+        quant_mx_compute_any<kF16, kTiled, true>(raw, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
+    }
 }
 
 // Materialize one chunk of SEGS segments (2 * SEGS blocks); all loads of the chunk are
