@@ -166,7 +166,10 @@ __device__ __forceinline__ float gather_amax(const float (&m)[SEGS], int lane)
 }
 
 // ---------------------------------------------------------------- quantize
-template <class Codec, int SEGS>
+// kRewiden: the chunk goes to the codec's requantization as its raw BF16 words, widened
+// again for each read (Bf16Vals), instead of as FP32 values widened once (RegVals);
+// fewer registers for one more widening.
+template <class Codec, int SEGS, bool kRewiden = false>
 struct QuantOp {
     const uint16_t *__restrict__ x;
     typename Codec::Q *__restrict__ q;
@@ -188,11 +191,15 @@ struct QuantOp {
     template <bool kTail>
     __device__ __forceinline__ void compute(const In &in, int64_t c) const
     {
-        float2 v[SEGS][4];
+        const int64_t e0 = c * (256 * SEGS) + lane * 8, b0 = c * (2 * SEGS);
+        if constexpr (kRewiden) {
+            Codec::template requant<SEGS, kTail, false>(Bf16Vals<SEGS>{in.x}, e0, b0, nblk, lane, q, s, nullptr);
+        } else {
+            float2 v[SEGS][4];
 #pragma unroll
-        for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
-        Codec::template requant<SEGS, kTail, false>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s,
-                                                    nullptr);
+            for (int j = 0; j < SEGS; j++) bf16x8_to_f32(in.x[j], v[j]);
+            Codec::template requant<SEGS, kTail, false>(RegVals<SEGS>{v}, e0, b0, nblk, lane, q, s, nullptr);
+        }
     }
     static constexpr uint32_t kStageBytes = 512u * SEGS;  // the chunk's BF16 values
     static_assert(kStageBytes % 16 == 0, "bulk copies move whole 16-byte units");
@@ -315,8 +322,8 @@ struct ReduceQuantOp {
             const uint4 rounded = f32x8_to_bf16x8(acc[j]);  // the reduce-scatter's BF16 result
             bf16x8_to_f32(rounded, acc[j]);
         }
-        Codec::template requant<SEGS, kTail, kOut>(acc, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q,
-                                                   s, out);
+        Codec::template requant<SEGS, kTail, kOut>(RegVals<SEGS>{acc}, c * (256 * SEGS) + lane * 8, c * (2 * SEGS),
+                                                   nblk, lane, q, s, out);
     }
 };
 
@@ -420,8 +427,8 @@ struct AccumOp {
             load_sources<SEGS, W, kTail>(more, src, g, nsrc, c, nblk, lane);
             add_sources<Codec, SEGS, W, false>(more, g, nsrc, acc, lane);
         }
-        Codec::template requant<SEGS, kTail, kOut>(acc, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q,
-                                                   s, out);
+        Codec::template requant<SEGS, kTail, kOut>(RegVals<SEGS>{acc}, c * (256 * SEGS) + lane * 8, c * (2 * SEGS),
+                                                   nblk, lane, q, s, out);
     }
 };
 
@@ -488,8 +495,8 @@ struct HopOp {
 #pragma unroll
             for (int e = 0; e < 4; e++) v[j][e] = add2(d[e], xl[e]);
         }
-        Codec::template requant<SEGS, kTail, kOut>(v, c * (256 * SEGS) + lane * 8, c * (2 * SEGS), nblk, lane, q, s,
-                                                   out);
+        Codec::template requant<SEGS, kTail, kOut>(RegVals<SEGS>{v}, c * (256 * SEGS) + lane * 8, c * (2 * SEGS),
+                                                   nblk, lane, q, s, out);
     }
 };
 

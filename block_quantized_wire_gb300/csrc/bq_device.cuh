@@ -228,6 +228,37 @@ __device__ __forceinline__ void f16x8_to_f32(const uint4 w, float2 (&v)[4])
     }
 }
 
+// The values of a warp chunk as a requantization reads them: seg(j, v) gives this
+// lane's eight values of segment j. RegVals holds FP32 values in registers (the sums of
+// the reductions). Bf16Vals holds the raw BF16 words of a quantize and widens them on
+// every read: a few integer operations per read instead of 16 registers per 4 segments.
+template <int SEGS>
+struct RegVals {
+    const float2 (&v)[SEGS][4];
+    __device__ __forceinline__ void seg(int j, float2 (&o)[4]) const
+    {
+#pragma unroll
+        for (int e = 0; e < 4; e++) o[e] = v[j][e];
+    }
+};
+
+template <int SEGS>
+struct Bf16Vals {
+    const uint4 (&x)[SEGS];
+    // volatile: each read widens anew, so the compiler cannot keep the first widening
+    // alive in place of the raw words
+    __device__ __forceinline__ void seg(int j, float2 (&o)[4]) const
+    {
+        const uint32_t u[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            uint32_t lo, hi;
+            asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(u[i]));
+            o[i] = make_float2(__uint_as_float(lo), __uint_as_float(hi));
+        }
+    }
+};
+
 __device__ __forceinline__ uint4 f32x8_to_bf16x8(const float2 (&v)[4])
 {
     return make_uint4(f32x2_to_bf16x2(v[0]), f32x2_to_bf16x2(v[1]), f32x2_to_bf16x2(v[2]), f32x2_to_bf16x2(v[3]));

@@ -16,15 +16,19 @@ namespace {
 
 // Requantize SEGS segments of FP32 values (v[j] = lane's 8 values of segment j):
 // writes the payload, the chunk's scales and, when kOut, the BF16 materialization.
-template <int SEGS, bool kTail, bool kOut>
-__device__ __forceinline__ void requant_chunk(const float2 (&v)[SEGS][4], int64_t e0, int64_t b0, int64_t nblk,
-                                              int lane, int8_t *__restrict__ q, float *__restrict__ s,
+template <int SEGS, bool kTail, bool kOut, class Vals>
+__device__ __forceinline__ void requant_chunk(const Vals &vals, int64_t e0, int64_t b0, int64_t nblk, int lane,
+                                              int8_t *__restrict__ q, float *__restrict__ s,
                                               uint16_t *__restrict__ out)
 {
     const int half = lane >> 4;
     float m[SEGS];
 #pragma unroll
-    for (int j = 0; j < SEGS; j++) m[j] = halfwarp_max(amax8(v[j]));
+    for (int j = 0; j < SEGS; j++) {
+        float2 v[4];
+        vals.seg(j, v);
+        m[j] = halfwarp_max(amax8(v));
+    }
     const I8Scale mine = i8_block_scale(gather_amax<SEGS>(m, lane));
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
@@ -32,8 +36,10 @@ __device__ __forceinline__ void requant_chunk(const float2 (&v)[SEGS][4], int64_
         bj.s = __shfl_sync(kFull, mine.s, 2 * j + half);
         bj.r = __shfl_sync(kFull, mine.r, 2 * j + half);
         bj.rl = __shfl_sync(kFull, mine.rl, 2 * j + half);
+        float2 v[4];
+        vals.seg(j, v);
         uint32_t w[8];
-        i8_quant8(v[j], bj, w);
+        i8_quant8(v, bj, w);
         if (!kTail || b0 + 2 * j + half < nblk) {
             st_v2(q + e0 + 256 * j, pack_payload8(w));
             if (kOut) st_v4(out + e0 + 256 * j, i8_materialize_words(w, bj.s));
@@ -56,11 +62,11 @@ struct I8Codec {
 #pragma unroll
         for (int e = 0; e < 4; e++) d[e] = mul2_unfused(v[e], s);
     }
-    template <int SEGS, bool kTail, bool kOut>
-    static __device__ __forceinline__ void requant(const float2 (&v)[SEGS][4], int64_t e0, int64_t b0, int64_t nblk,
-                                                   int lane, int8_t *q, float *s, uint16_t *out)
+    template <int SEGS, bool kTail, bool kOut, class Vals>
+    static __device__ __forceinline__ void requant(const Vals &vals, int64_t e0, int64_t b0, int64_t nblk, int lane,
+                                                   int8_t *q, float *s, uint16_t *out)
     {
-        requant_chunk<SEGS, kTail, kOut>(v, e0, b0, nblk, lane, q, s, out);
+        requant_chunk<SEGS, kTail, kOut>(vals, e0, b0, nblk, lane, q, s, out);
     }
     static __device__ __forceinline__ uint4 dequant8(uint2 q, uint32_t word, int)
     {

@@ -19,9 +19,9 @@ namespace {
 // L holds the amax of the chunk's group L (block L/4, group L%4 of that block) and
 // computes its E8M0 byte and multipliers once; each lane then fetches its own group's
 // multiplier per segment, and lanes 4b store block b's four scale bytes as one word.
-template <int SEGS, bool kTail, bool kOut>
-__device__ __forceinline__ void requant_mx_chunk(const float2 (&v)[SEGS][4], int64_t e0, int64_t b0, int64_t nblk,
-                                                 int lane, uint8_t *__restrict__ q, uint32_t *__restrict__ s,
+template <int SEGS, bool kTail, bool kOut, class Vals>
+__device__ __forceinline__ void requant_mx_chunk(const Vals &vals, int64_t e0, int64_t b0, int64_t nblk, int lane,
+                                                 uint8_t *__restrict__ q, uint32_t *__restrict__ s,
                                                  uint16_t *__restrict__ out)
 {
     static_assert(8 * SEGS <= 32, "a chunk's groups fit one per lane");
@@ -29,7 +29,9 @@ __device__ __forceinline__ void requant_mx_chunk(const float2 (&v)[SEGS][4], int
     float gmax = 0.0f;
 #pragma unroll
     for (int j = 0; j < SEGS; j++) {
-        float m = amax8(v[j]);
+        float2 v[4];
+        vals.seg(j, v);
+        float m = amax8(v);
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
         const float g = __shfl_sync(kFull, m, (lane & 7) << 2);
@@ -43,9 +45,10 @@ __device__ __forceinline__ void requant_mx_chunk(const float2 (&v)[SEGS][4], int
         const int src = 8 * j + (lane >> 2);
         const float2 pj = splat(__shfl_sync(kFull, p, src));
         const float pinv_j = kOut ? __shfl_sync(kFull, pinv, src) : 0.0f;
-        float2 y[4];
+        float2 v[4], y[4];
+        vals.seg(j, v);
 #pragma unroll
-        for (int i = 0; i < 4; i++) y[i] = mul2(v[j][i], pj);  // exact: a power-of-two scaling
+        for (int i = 0; i < 4; i++) y[i] = mul2(v[i], pj);  // exact: a power-of-two scaling
         const uint2 codes = f32x8_to_e4m3x8(y);
         if (!kTail || b0 + 2 * j + half < nblk) {
             st_v2(q + e0 + 256 * j, codes);
@@ -73,11 +76,11 @@ struct MxCodec {
         const float p = e == 255u ? __uint_as_float(0x7fc00000u) : exp2i(static_cast<int>(e) - 127);
         e4m3x8_to_f32(q, p, d);
     }
-    template <int SEGS, bool kTail, bool kOut>
-    static __device__ __forceinline__ void requant(const float2 (&v)[SEGS][4], int64_t e0, int64_t b0, int64_t nblk,
+    template <int SEGS, bool kTail, bool kOut, class Vals>
+    static __device__ __forceinline__ void requant(const Vals &vals, int64_t e0, int64_t b0, int64_t nblk,
                                                    int lane, uint8_t *q, uint32_t *s, uint16_t *out)
     {
-        requant_mx_chunk<SEGS, kTail, kOut>(v, e0, b0, nblk, lane, q, s, out);
+        requant_mx_chunk<SEGS, kTail, kOut>(vals, e0, b0, nblk, lane, q, s, out);
     }
 };
 
