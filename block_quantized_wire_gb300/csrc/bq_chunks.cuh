@@ -374,7 +374,10 @@ __device__ __forceinline__ void add_sources(const SourceRegs<SEGS, W> &r, int g,
     }
 }
 
-template <class Codec, int SEGS, int W, bool kOut>
+// kMore: the call may have more than W sources, added W at a time after the first
+// group; without it the operation serves nsrc <= W and keeps no registers for a
+// second group (the four-source kernel spilled with them).
+template <class Codec, int SEGS, int W, bool kOut, bool kMore = true>
 struct AccumOp {
     using Q = typename Codec::Q;
     using S = typename Codec::S;
@@ -422,10 +425,12 @@ struct AccumOp {
     {
         float2 acc[SEGS][4];
         add_sources<Codec, SEGS, W, true>(in, 0, nsrc, acc, lane);
-        for (int g = W; g < nsrc; g += W) {
-            In more;
-            load_sources<SEGS, W, kTail>(more, src, g, nsrc, c, nblk, lane);
-            add_sources<Codec, SEGS, W, false>(more, g, nsrc, acc, lane);
+        if constexpr (kMore) {
+            for (int g = W; g < nsrc; g += W) {
+                In more;
+                load_sources<SEGS, W, kTail>(more, src, g, nsrc, c, nblk, lane);
+                add_sources<Codec, SEGS, W, false>(more, g, nsrc, acc, lane);
+            }
         }
         Codec::template requant<SEGS, kTail, kOut>(RegVals<SEGS>{acc}, c * (256 * SEGS) + lane * 8, c * (2 * SEGS),
                                                    nblk, lane, q, s, out);

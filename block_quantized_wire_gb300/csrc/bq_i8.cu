@@ -120,32 +120,32 @@ dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int
 }
 
 // ---------------------------------------------------------------- accumulate
-template <int SEGS, int W, bool kOut>
-using AccumI8 = AccumOp<I8Codec, SEGS, W, kOut>;
+template <int SEGS, int W, bool kOut, bool kMore>
+using AccumI8 = AccumOp<I8Codec, SEGS, W, kOut, kMore>;
 
 #ifndef BQ_ACCUM_MIN_CTAS
 #define BQ_ACCUM_MIN_CTAS 3
 #endif
 
-template <int SEGS, int W, bool kOut, int STAGES>
+template <int SEGS, int W, bool kOut, bool kMore, int STAGES>
 __global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
 accum_i8_staged_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
                        float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
     extern __shared__ __align__(128) unsigned char smem[];
-    const AccumI8<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    const AccumI8<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_staged<STAGES>(op, nblk, 2 * SEGS,
-                       smem + (threadIdx.x >> 5) * staged_warp_bytes<AccumI8<SEGS, W, kOut>, STAGES>());
+                       smem + (threadIdx.x >> 5) * staged_warp_bytes<AccumI8<SEGS, W, kOut, kMore>, STAGES>());
 }
 
-template <int SEGS, int W, bool kOut>
+template <int SEGS, int W, bool kOut, bool kMore>
 __global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
 accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s,
                 uint16_t *__restrict__ out)
 {
     pdl_begin();
-    const AccumI8<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    const AccumI8<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
@@ -224,7 +224,7 @@ constexpr int kStagesQuant = BQ_STAGES_QUANT;
 constexpr int kStagesHop = BQ_STAGES_HOP;
 constexpr int kStagesAccum = BQ_STAGES_ACCUM;
 
-template <int W, bool kOut>
+template <int W, bool kOut, bool kMore>
 cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                            cudaStream_t st)
 {
@@ -234,11 +234,11 @@ cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t
         bool staged = true;
         for (int i = 0; i < W && i < nsrc; i++) staged = staged && aligned16(src.s[i]);
         if (staged)
-            return launch_staged<AccumI8<kSegsAccum, W, kOut>, kStagesAccum>(
-                accum_i8_staged_kernel<kSegsAccum, W, kOut, kStagesAccum>, chunks(nblk, kSegsAccum), st, src, nsrc,
-                nblk, q, s, out);
+            return launch_staged<AccumI8<kSegsAccum, W, kOut, kMore>, kStagesAccum>(
+                accum_i8_staged_kernel<kSegsAccum, W, kOut, kMore, kStagesAccum>, chunks(nblk, kSegsAccum), st, src,
+                nsrc, nblk, q, s, out);
     }
-    auto kernel = accum_i8_kernel<kSegsAccum, W, kOut>;
+    auto kernel = accum_i8_kernel<kSegsAccum, W, kOut, kMore>;
     BQK_GRID(kernel, chunks(nblk, kSegsAccum));
     return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
 }
@@ -303,12 +303,22 @@ cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uin
 cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                             cudaStream_t st)
 {
+    // Four sources without the owner output take a kernel without the extra-group path:
+    // 439 us against 441 us per 469.8M-value launch on GB300. With the owner output the
+    // same kernel was slower (34.3 against 27.4 us at 3072x7168), so there, and for
+    // other widths, the general kernel stays.
     const bool o = out != nullptr;
     switch (W) {
-    case 1: return o ? launch_accum_w<1, true>(src, W, nblk, q, s, out, st) : launch_accum_w<1, false>(src, W, nblk, q, s, out, st);
-    case 2: return o ? launch_accum_w<2, true>(src, W, nblk, q, s, out, st) : launch_accum_w<2, false>(src, W, nblk, q, s, out, st);
-    case 3: return o ? launch_accum_w<3, true>(src, W, nblk, q, s, out, st) : launch_accum_w<3, false>(src, W, nblk, q, s, out, st);
-    default: return o ? launch_accum_w<4, true>(src, W, nblk, q, s, out, st) : launch_accum_w<4, false>(src, W, nblk, q, s, out, st);
+    case 1: return o ? launch_accum_w<1, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_w<1, false, true>(src, W, nblk, q, s, out, st);
+    case 2: return o ? launch_accum_w<2, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_w<2, false, true>(src, W, nblk, q, s, out, st);
+    case 3: return o ? launch_accum_w<3, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_w<3, false, true>(src, W, nblk, q, s, out, st);
+    case 4: return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_w<4, false, false>(src, W, nblk, q, s, out, st);
+    default: return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
+                      : launch_accum_w<4, false, true>(src, W, nblk, q, s, out, st);
     }
 }
 

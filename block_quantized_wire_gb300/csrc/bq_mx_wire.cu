@@ -84,8 +84,8 @@ struct MxCodec {
     }
 };
 
-template <int SEGS, int W, bool kOut>
-using AccumMx = AccumOp<MxCodec, SEGS, W, kOut>;
+template <int SEGS, int W, bool kOut, bool kMore>
+using AccumMx = AccumOp<MxCodec, SEGS, W, kOut, kMore>;
 template <int SEGS, bool kOut>
 using HopMx = HopOp<MxCodec, SEGS, kOut>;
 
@@ -93,25 +93,26 @@ using HopMx = HopOp<MxCodec, SEGS, kOut>;
 #define BQ_ACCUM_MX_MIN_CTAS 3
 #endif
 
-template <int SEGS, int W, bool kOut>
+template <int SEGS, int W, bool kOut, bool kMore>
 __global__ void __launch_bounds__(kThreads, BQ_ACCUM_MX_MIN_CTAS)
 accum_mx_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t nblk, uint8_t *__restrict__ q,
                 uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
-    const AccumMx<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    const AccumMx<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
-template <int SEGS, int W, bool kOut, int STAGES>
+template <int SEGS, int W, bool kOut, bool kMore, int STAGES>
 __global__ void __launch_bounds__(kThreads, BQ_ACCUM_MX_MIN_CTAS)
 accum_mx_staged_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t nblk, uint8_t *__restrict__ q,
                        uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
     extern __shared__ __align__(128) unsigned char smem[];
-    const AccumMx<SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
-    run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<AccumMx<SEGS, W, kOut>, STAGES>());
+    const AccumMx<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_staged<STAGES>(op, nblk, 2 * SEGS,
+                       smem + (threadIdx.x >> 5) * staged_warp_bytes<AccumMx<SEGS, W, kOut, kMore>, STAGES>());
 }
 
 template <int SEGS, bool kOut>
@@ -154,7 +155,7 @@ constexpr int kSegsHopMx = BQ_SEGS_HOP_MX;
 constexpr int kStagesAccumMx = BQ_STAGES_ACCUM_MX;
 constexpr int kStagesHopMx = BQ_STAGES_HOP_MX;
 
-template <int W, bool kOut>
+template <int W, bool kOut, bool kMore>
 cudaError_t launch_accum_mx_w(const MxSourceList &src, int nsrc, int64_t nblk, uint8_t *q, uint32_t *s,
                               uint16_t *out, cudaStream_t st)
 {
@@ -163,11 +164,11 @@ cudaError_t launch_accum_mx_w(const MxSourceList &src, int nsrc, int64_t nblk, u
         bool staged = true;
         for (int i = 0; i < W && i < nsrc; i++) staged = staged && aligned16(src.s[i]);
         if (staged)
-            return launch_staged<AccumMx<kSegsAccumMx, W, kOut>, kStagesAccumMx>(
-                accum_mx_staged_kernel<kSegsAccumMx, W, kOut, kStagesAccumMx>, chunks(nblk, kSegsAccumMx), st, src,
-                nsrc, nblk, q, s, out);
+            return launch_staged<AccumMx<kSegsAccumMx, W, kOut, kMore>, kStagesAccumMx>(
+                accum_mx_staged_kernel<kSegsAccumMx, W, kOut, kMore, kStagesAccumMx>, chunks(nblk, kSegsAccumMx), st,
+                src, nsrc, nblk, q, s, out);
     }
-    auto kernel = accum_mx_kernel<kSegsAccumMx, W, kOut>;
+    auto kernel = accum_mx_kernel<kSegsAccumMx, W, kOut, kMore>;
     BQK_GRID(kernel, chunks(nblk, kSegsAccumMx));
     return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
 }
@@ -195,10 +196,14 @@ cudaError_t launch_accum_mx(const MxSourceList &src, int W, int64_t nblk, uint8_
 {
     const bool o = out != nullptr;
     switch (W) {
-    case 1: return o ? launch_accum_mx_w<1, true>(src, W, nblk, q, s, out, st) : launch_accum_mx_w<1, false>(src, W, nblk, q, s, out, st);
-    case 2: return o ? launch_accum_mx_w<2, true>(src, W, nblk, q, s, out, st) : launch_accum_mx_w<2, false>(src, W, nblk, q, s, out, st);
-    case 3: return o ? launch_accum_mx_w<3, true>(src, W, nblk, q, s, out, st) : launch_accum_mx_w<3, false>(src, W, nblk, q, s, out, st);
-    default: return o ? launch_accum_mx_w<4, true>(src, W, nblk, q, s, out, st) : launch_accum_mx_w<4, false>(src, W, nblk, q, s, out, st);
+    case 1: return o ? launch_accum_mx_w<1, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_mx_w<1, false, true>(src, W, nblk, q, s, out, st);
+    case 2: return o ? launch_accum_mx_w<2, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_mx_w<2, false, true>(src, W, nblk, q, s, out, st);
+    case 3: return o ? launch_accum_mx_w<3, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_mx_w<3, false, true>(src, W, nblk, q, s, out, st);
+    default: return o ? launch_accum_mx_w<4, true, true>(src, W, nblk, q, s, out, st)
+                      : launch_accum_mx_w<4, false, true>(src, W, nblk, q, s, out, st);
     }
 }
 
