@@ -149,6 +149,119 @@ accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, 
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
+// ---------------------------------------------------------------- accumulate, wide lanes
+// The accumulate of up to W sources without the owner output, laid out for fewer
+// instructions per value. A lane takes 16 consecutive values (one 16-byte payload load
+// per source) instead of 8, so a 128-value block spans 8 lanes; a warp chunk is two
+// such 512-value segments, the same 8 blocks as the 4-segment layout. The block amax
+// then takes a 3-step butterfly over twice the values per lane, and the scale shuffles,
+// the loads and the payload stores halve. The arithmetic and its order are AccumOp's:
+// d = fl(q * s) per source, summed in source order, then requantized.
+__device__ __forceinline__ float octet_max(float m)
+{
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+    return m;
+}
+
+template <int W>
+struct AccumWideI8 {
+    const SourceList &src;  // the kernel's __grid_constant__ parameter, read in place
+    int nsrc;
+    int8_t *__restrict__ q;
+    float *__restrict__ s;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint4 q[W][2];
+        uint32_t sc[W];  // lanes 0..7: the scales of the chunk's blocks 0..7
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
+        const int g = lane >> 3;
+        const bool lane_ok = lane < 8 && (!kTail || b0 + lane < nblk);
+#pragma unroll
+        for (int i = 0; i < W; i++) {
+            const bool src_ok = i < nsrc;
+            const int8_t *qw = src.q[src_ok ? i : 0];
+            const float *sw = src.s[src_ok ? i : 0];
+#pragma unroll
+            for (int j = 0; j < 2; j++)
+                in.q[i][j] = (src_ok && (!kTail || b0 + 4 * j + g < nblk)) ? ld_stream_v4(qw + e0 + 512 * j)
+                                                                           : make_uint4(0, 0, 0, 0);
+            in.sc[i] = (src_ok && lane_ok) ? ld_stream_u32(sw + b0 + lane) : 0u;
+        }
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
+        const int g = lane >> 3;
+        float2 acc[2][2][4];  // [segment][half of the lane's 16 values][pair]
+#pragma unroll
+        for (int i = 0; i < W; i++) {
+            if (i >= nsrc) break;
+#pragma unroll
+            for (int j = 0; j < 2; j++) {
+                const float2 sc = splat(__uint_as_float(__shfl_sync(kFull, in.sc[i], 4 * j + g)));
+                float2 v[2][4];
+                i8x8_to_f32(make_uint2(in.q[i][j].x, in.q[i][j].y), v[0]);
+                i8x8_to_f32(make_uint2(in.q[i][j].z, in.q[i][j].w), v[1]);
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const float2 d = mul2_unfused(v[h][e], sc);
+                        acc[j][h][e] = i == 0 ? d : add2(acc[j][h][e], d);
+                    }
+            }
+        }
+        float m[2];
+#pragma unroll
+        for (int j = 0; j < 2; j++) m[j] = octet_max(fmaxf(amax8(acc[j][0]), amax8(acc[j][1])));
+        // lane b < 8 computes the scale of the chunk's block b: segment b / 4, lane group b % 4
+        float mine = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const float gm = __shfl_sync(kFull, m[j], (lane & 3) << 3);
+            if ((lane >> 2) == j) mine = gm;
+        }
+        const I8Scale sb = i8_block_scale(mine);
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            I8Scale bj;
+            bj.s = __shfl_sync(kFull, sb.s, 4 * j + g);
+            bj.r = __shfl_sync(kFull, sb.r, 4 * j + g);
+            bj.rl = __shfl_sync(kFull, sb.rl, 4 * j + g);
+            uint32_t w0[8], w1[8];
+            i8_quant8(acc[j][0], bj, w0);
+            i8_quant8(acc[j][1], bj, w1);
+            if (!kTail || b0 + 4 * j + g < nblk) {
+                const uint2 p0 = pack_payload8(w0), p1 = pack_payload8(w1);
+                st_v4(q + e0 + 512 * j, make_uint4(p0.x, p0.y, p1.x, p1.y));
+            }
+        }
+        if (lane < 8 && (!kTail || b0 + lane < nblk)) s[b0 + lane] = sb.s;
+    }
+};
+
+#ifndef BQ_ACCUM_WIDE
+#define BQ_ACCUM_WIDE 1
+#endif
+
+template <int W>
+__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
+accum_i8_wide_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
+                     float *__restrict__ s)
+{
+    pdl_begin();
+    const AccumWideI8<W> op{src, nsrc, q, s, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 8);
+}
+
 // ---------------------------------------------------------------- ring hop
 template <int SEGS, bool kOut>
 using HopI8 = HopOp<I8Codec, SEGS, kOut>;
@@ -315,8 +428,13 @@ cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *
                    : launch_accum_w<2, false, true>(src, W, nblk, q, s, out, st);
     case 3: return o ? launch_accum_w<3, true, true>(src, W, nblk, q, s, out, st)
                    : launch_accum_w<3, false, true>(src, W, nblk, q, s, out, st);
-    case 4: return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
-                   : launch_accum_w<4, false, false>(src, W, nblk, q, s, out, st);
+    case 4:
+        if (!o && BQ_ACCUM_WIDE) {
+            BQK_GRID(accum_i8_wide_kernel<4>, chunks(nblk, 4));
+            return launch_kernel(accum_i8_wide_kernel<4>, grid, st, src, W, nblk, q, s);
+        }
+        return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
+                 : launch_accum_w<4, false, false>(src, W, nblk, q, s, out, st);
     default: return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
                       : launch_accum_w<4, false, true>(src, W, nblk, q, s, out, st);
     }

@@ -188,22 +188,28 @@ def test_dequant_arbitrary_payloads():
     assert_same(out, oracle.dequant_i8(q, s), "materialized")
 
 
+@pytest.mark.parametrize("owner", [True, False])
 @pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 7, 8, 9, 16])
-def test_accumulate_any_width(W):
-    rng = np.random.default_rng(100 + W)
-    nblk = 37
+@pytest.mark.parametrize("nblk", [37, 8, 1])
+def test_accumulate_any_width(W, owner, nblk):
+    # with and without the owner output (separate kernels), whole and partial chunks
+    rng = np.random.default_rng(100 + W + nblk)
     xs = [adversarial_blocks(rng, nblk, max_abs=1.0e37).reshape(-1) for _ in range(W)]  # sums stay finite
     ref = [oracle.quant_i8(x) for x in xs]
     qd = [torch.from_numpy(r[0]).cuda() for r in ref]
     sd = [torch.from_numpy(r[1]).cuda() for r in ref]
     n = nblk * 128
     gq, gs, go = Guarded(n), Guarded(4 * nblk), Guarded(2 * n)
-    codec.dequant_accum_i8(qd, sd, gq.view(torch.int8), gs.view(torch.float32), go.view(torch.bfloat16))
+    codec.dequant_accum_i8(qd, sd, gq.view(torch.int8), gs.view(torch.float32),
+                           go.view(torch.bfloat16) if owner else None)
     qa, sa, oa = oracle.dequant_accum_i8([r[0] for r in ref], [r[1] for r in ref], materialize=True)
     assert np.all(np.isfinite(sa))
     assert_same(gq.view(torch.int8), qa, "payload")
     assert_same(gs.view(torch.float32), sa, "scales")
-    assert_same(go.view(torch.bfloat16), oa, "materialized")
+    if owner:
+        assert_same(go.view(torch.bfloat16), oa, "materialized")
+    else:
+        assert (go.raw == Guarded.SENTINEL).all().item()  # no owner output: nothing written
     assert gq.bands_intact() and gs.bands_intact() and go.bands_intact()
 
 
@@ -227,13 +233,18 @@ def test_accumulate_repeated_source_and_tiny_sums():
     s[5] = np.float32(1.0)
     q = q.reshape(-1)
     qd, sd = torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda()
-    _, qo, so = codec.empty_wire_i8(q.size)
-    out = torch.empty(q.size, dtype=torch.bfloat16, device="cuda")
-    codec.dequant_accum_i8([qd, qd, qd], [sd, sd, sd], qo, so, out)
-    qa, sa, oa = oracle.dequant_accum_i8([q, q, q], [s, s, s], materialize=True)
-    assert_same(qo, qa, "payload")
-    assert_same(so, sa, "scales")
-    assert_same(out, oa, "materialized")
+    for W in (3, 4):  # three sources, and four (the kernel without the owner output too)
+        _, qo, so = codec.empty_wire_i8(q.size)
+        out = torch.empty(q.size, dtype=torch.bfloat16, device="cuda")
+        codec.dequant_accum_i8([qd] * W, [sd] * W, qo, so, out)
+        qa, sa, oa = oracle.dequant_accum_i8([q] * W, [s] * W, materialize=True)
+        assert_same(qo, qa, "payload")
+        assert_same(so, sa, "scales")
+        assert_same(out, oa, "materialized")
+        _, qn, sn = codec.empty_wire_i8(q.size)
+        codec.dequant_accum_i8([qd] * W, [sd] * W, qn, sn, None)
+        assert_same(qn, qa, "payload without owner output")
+        assert_same(sn, sa, "scales without owner output")
 
 
 def test_ring_hop_edge_cases():
