@@ -149,14 +149,13 @@ accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, 
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
 
-// ---------------------------------------------------------------- accumulate, wide lanes
-// The accumulate of up to W sources without the owner output, laid out for fewer
-// instructions per value. A lane takes 16 consecutive values (one 16-byte payload load
-// per source) instead of 8, so a 128-value block spans 8 lanes; a warp chunk is two
-// such 512-value segments, the same 8 blocks as the 4-segment layout. The block amax
-// then takes a 3-step butterfly over twice the values per lane, and the scale shuffles,
-// the loads and the payload stores halve. The arithmetic and its order are AccumOp's:
-// d = fl(q * s) per source, summed in source order, then requantized.
+// ---------------------------------------------------------------- wide lanes
+// Quantize and accumulate laid out for fewer instructions per value. A lane takes 16
+// consecutive values (one 16-byte payload word, two 16-byte BF16 words) instead of 8,
+// so a 128-value block spans 8 lanes; a warp chunk is two such 512-value segments, the
+// same 8 blocks as the 4-segment layout. The block amax then takes a 3-step butterfly
+// over twice the values per lane, and the scale shuffles, the loads and the payload
+// stores halve per value. The arithmetic and its order are those of the 8-value layout.
 __device__ __forceinline__ float octet_max(float m)
 {
     m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
@@ -165,12 +164,89 @@ __device__ __forceinline__ float octet_max(float m)
     return m;
 }
 
-template <int W>
+// Requantize one wide chunk: v[j][h] are the lane's values 8h..8h+7 of segment j
+// (elements e0 + 512 j + 8 h ...), whose block is b0 + 4 j + (lane >> 3). Writes the
+// payload, the chunk's 8 scales and, when kOut, the BF16 materialization.
+template <bool kTail, bool kOut>
+__device__ __forceinline__ void requant_wide(const float2 (&v)[2][2][4], int64_t e0, int64_t b0, int64_t nblk,
+                                             int lane, int8_t *__restrict__ q, float *__restrict__ s,
+                                             uint16_t *__restrict__ out)
+{
+    const int g = lane >> 3;
+    float m[2];
+#pragma unroll
+    for (int j = 0; j < 2; j++) m[j] = octet_max(fmaxf(amax8(v[j][0]), amax8(v[j][1])));
+    // lane b < 8 computes the scale of the chunk's block b: segment b / 4, lane group b % 4
+    float mine = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const float gm = __shfl_sync(kFull, m[j], (lane & 3) << 3);
+        if ((lane >> 2) == j) mine = gm;
+    }
+    const I8Scale sb = i8_block_scale(mine);
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        I8Scale bj;
+        bj.s = __shfl_sync(kFull, sb.s, 4 * j + g);
+        bj.r = __shfl_sync(kFull, sb.r, 4 * j + g);
+        bj.rl = __shfl_sync(kFull, sb.rl, 4 * j + g);
+        uint32_t w0[8], w1[8];
+        i8_quant8(v[j][0], bj, w0);
+        i8_quant8(v[j][1], bj, w1);
+        if (!kTail || b0 + 4 * j + g < nblk) {
+            const uint2 p0 = pack_payload8(w0), p1 = pack_payload8(w1);
+            st_v4(q + e0 + 512 * j, make_uint4(p0.x, p0.y, p1.x, p1.y));
+            if (kOut) {
+                st_v4(out + e0 + 512 * j, i8_materialize_words(w0, bj.s));
+                st_v4(out + e0 + 512 * j + 8, i8_materialize_words(w1, bj.s));
+            }
+        }
+    }
+    if (lane < 8 && (!kTail || b0 + lane < nblk)) s[b0 + lane] = sb.s;
+}
+
+// Quantize: the lane's 16 BF16 values are two 16-byte words per segment.
+struct QuantWideI8 {
+    const uint16_t *__restrict__ x;
+    int8_t *__restrict__ q;
+    float *__restrict__ s;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint4 x[2][2];
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const bool ok = !kTail || b0 + 4 * j + (lane >> 3) < nblk;
+#pragma unroll
+            for (int h = 0; h < 2; h++)
+                in.x[j][h] = ok ? ld_stream_v4(x + e0 + 512 * j + 8 * h) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float2 v[2][2][4];
+#pragma unroll
+        for (int j = 0; j < 2; j++)
+#pragma unroll
+            for (int h = 0; h < 2; h++) bf16x8_to_f32(in.x[j][h], v[j][h]);
+        requant_wide<kTail, false>(v, c * 1024 + lane * 16, c * 8, nblk, lane, q, s, nullptr);
+    }
+};
+
+// Accumulate of W sources at a time (kMore: further groups of W follow the first).
+template <int W, bool kOut, bool kMore>
 struct AccumWideI8 {
     const SourceList &src;  // the kernel's __grid_constant__ parameter, read in place
     int nsrc;
     int8_t *__restrict__ q;
     float *__restrict__ s;
+    uint16_t *__restrict__ out;
     int64_t nblk;
     int lane;
     struct In {
@@ -178,16 +254,16 @@ struct AccumWideI8 {
         uint32_t sc[W];  // lanes 0..7: the scales of the chunk's blocks 0..7
     };
     template <bool kTail>
-    __device__ __forceinline__ void load(In &in, int64_t c) const
+    __device__ __forceinline__ void load_group(In &in, int gsrc, int64_t c) const
     {
         const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
         const int g = lane >> 3;
         const bool lane_ok = lane < 8 && (!kTail || b0 + lane < nblk);
 #pragma unroll
         for (int i = 0; i < W; i++) {
-            const bool src_ok = i < nsrc;
-            const int8_t *qw = src.q[src_ok ? i : 0];
-            const float *sw = src.s[src_ok ? i : 0];
+            const bool src_ok = gsrc + i < nsrc;
+            const int8_t *qw = src.q[src_ok ? gsrc + i : gsrc];
+            const float *sw = src.s[src_ok ? gsrc + i : gsrc];
 #pragma unroll
             for (int j = 0; j < 2; j++)
                 in.q[i][j] = (src_ok && (!kTail || b0 + 4 * j + g < nblk)) ? ld_stream_v4(qw + e0 + 512 * j)
@@ -196,14 +272,17 @@ struct AccumWideI8 {
         }
     }
     template <bool kTail>
-    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    __device__ __forceinline__ void load(In &in, int64_t c) const
     {
-        const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
+        load_group<kTail>(in, 0, c);
+    }
+    template <bool kFirst>
+    __device__ __forceinline__ void add_group(const In &in, int gsrc, float2 (&acc)[2][2][4]) const
+    {
         const int g = lane >> 3;
-        float2 acc[2][2][4];  // [segment][half of the lane's 16 values][pair]
 #pragma unroll
         for (int i = 0; i < W; i++) {
-            if (i >= nsrc) break;
+            if (gsrc + i >= nsrc) break;
 #pragma unroll
             for (int j = 0; j < 2; j++) {
                 const float2 sc = splat(__uint_as_float(__shfl_sync(kFull, in.sc[i], 4 * j + g)));
@@ -215,50 +294,49 @@ struct AccumWideI8 {
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
                         const float2 d = mul2_unfused(v[h][e], sc);
-                        acc[j][h][e] = i == 0 ? d : add2(acc[j][h][e], d);
+                        acc[j][h][e] = (kFirst && i == 0) ? d : add2(acc[j][h][e], d);
                     }
             }
         }
-        float m[2];
-#pragma unroll
-        for (int j = 0; j < 2; j++) m[j] = octet_max(fmaxf(amax8(acc[j][0]), amax8(acc[j][1])));
-        // lane b < 8 computes the scale of the chunk's block b: segment b / 4, lane group b % 4
-        float mine = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 2; j++) {
-            const float gm = __shfl_sync(kFull, m[j], (lane & 3) << 3);
-            if ((lane >> 2) == j) mine = gm;
-        }
-        const I8Scale sb = i8_block_scale(mine);
-#pragma unroll
-        for (int j = 0; j < 2; j++) {
-            I8Scale bj;
-            bj.s = __shfl_sync(kFull, sb.s, 4 * j + g);
-            bj.r = __shfl_sync(kFull, sb.r, 4 * j + g);
-            bj.rl = __shfl_sync(kFull, sb.rl, 4 * j + g);
-            uint32_t w0[8], w1[8];
-            i8_quant8(acc[j][0], bj, w0);
-            i8_quant8(acc[j][1], bj, w1);
-            if (!kTail || b0 + 4 * j + g < nblk) {
-                const uint2 p0 = pack_payload8(w0), p1 = pack_payload8(w1);
-                st_v4(q + e0 + 512 * j, make_uint4(p0.x, p0.y, p1.x, p1.y));
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float2 acc[2][2][4];  // [segment][half of the lane's 16 values][pair]
+        add_group<true>(in, 0, acc);
+        if constexpr (kMore) {
+            for (int gsrc = W; gsrc < nsrc; gsrc += W) {
+                In more;
+                load_group<kTail>(more, gsrc, c);
+                add_group<false>(more, gsrc, acc);
             }
         }
-        if (lane < 8 && (!kTail || b0 + lane < nblk)) s[b0 + lane] = sb.s;
+        requant_wide<kTail, kOut>(acc, c * 1024 + lane * 16, c * 8, nblk, lane, q, s, out);
     }
 };
 
 #ifndef BQ_ACCUM_WIDE
 #define BQ_ACCUM_WIDE 1
 #endif
+#ifndef BQ_QUANT_WIDE
+#define BQ_QUANT_WIDE 1
+#endif
 
-template <int W>
+template <int W, bool kOut, bool kMore>
 __global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
 accum_i8_wide_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
-                     float *__restrict__ s)
+                     float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
-    const AccumWideI8<W> op{src, nsrc, q, s, nblk, (int)(threadIdx.x & 31)};
+    const AccumWideI8<W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 8);
+}
+
+__global__ void __launch_bounds__(kThreads, BQ_QUANT_MIN_CTAS)
+quant_i8_wide_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
+{
+    pdl_begin();
+    const QuantWideI8 op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 8);
 }
 
@@ -338,6 +416,15 @@ constexpr int kStagesHop = BQ_STAGES_HOP;
 constexpr int kStagesAccum = BQ_STAGES_ACCUM;
 
 template <int W, bool kOut, bool kMore>
+cudaError_t launch_accum_wide(const SourceList &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
+                              cudaStream_t st)
+{
+    auto kernel = accum_i8_wide_kernel<W, kOut, kMore>;
+    BQK_GRID(kernel, chunks(nblk, 4));
+    return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
+}
+
+template <int W, bool kOut, bool kMore>
 cudaError_t launch_accum_w(const SourceList &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                            cudaStream_t st)
 {
@@ -372,6 +459,10 @@ cudaError_t launch_quant_stages(const uint16_t *x, int64_t nblk, int8_t *q, floa
 
 cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s, cudaStream_t st)
 {
+    if (BQ_QUANT_WIDE) {
+        BQK_GRID(quant_i8_wide_kernel, chunks(nblk, 4));
+        return launch_kernel(quant_i8_wide_kernel, grid, st, x, nblk, q, s);
+    }
     return launch_quant_stages<kStagesQuant>(x, nblk, q, s, st);
 }
 
@@ -416,11 +507,21 @@ cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uin
 cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                             cudaStream_t st)
 {
-    // Four sources without the owner output take a kernel without the extra-group path:
-    // 439 us against 441 us per 469.8M-value launch on GB300. With the owner output the
-    // same kernel was slower (34.3 against 27.4 us at 3072x7168), so there, and for
-    // other widths, the general kernel stays.
     const bool o = out != nullptr;
+    if (BQ_ACCUM_WIDE) {
+        switch (W) {
+        case 1: return o ? launch_accum_wide<1, true, false>(src, W, nblk, q, s, out, st)
+                       : launch_accum_wide<1, false, false>(src, W, nblk, q, s, out, st);
+        case 2: return o ? launch_accum_wide<2, true, false>(src, W, nblk, q, s, out, st)
+                       : launch_accum_wide<2, false, false>(src, W, nblk, q, s, out, st);
+        case 3: return o ? launch_accum_wide<3, true, false>(src, W, nblk, q, s, out, st)
+                       : launch_accum_wide<3, false, false>(src, W, nblk, q, s, out, st);
+        case 4: return o ? launch_accum_wide<4, true, false>(src, W, nblk, q, s, out, st)
+                       : launch_accum_wide<4, false, false>(src, W, nblk, q, s, out, st);
+        default: return o ? launch_accum_wide<4, true, true>(src, W, nblk, q, s, out, st)
+                          : launch_accum_wide<4, false, true>(src, W, nblk, q, s, out, st);
+        }
+    }
     switch (W) {
     case 1: return o ? launch_accum_w<1, true, true>(src, W, nblk, q, s, out, st)
                    : launch_accum_w<1, false, true>(src, W, nblk, q, s, out, st);
@@ -428,13 +529,8 @@ cudaError_t launch_accum_i8(const SourceList &src, int W, int64_t nblk, int8_t *
                    : launch_accum_w<2, false, true>(src, W, nblk, q, s, out, st);
     case 3: return o ? launch_accum_w<3, true, true>(src, W, nblk, q, s, out, st)
                    : launch_accum_w<3, false, true>(src, W, nblk, q, s, out, st);
-    case 4:
-        if (!o && BQ_ACCUM_WIDE) {
-            BQK_GRID(accum_i8_wide_kernel<4>, chunks(nblk, 4));
-            return launch_kernel(accum_i8_wide_kernel<4>, grid, st, src, W, nblk, q, s);
-        }
-        return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
-                 : launch_accum_w<4, false, false>(src, W, nblk, q, s, out, st);
+    case 4: return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
+                   : launch_accum_w<4, false, false>(src, W, nblk, q, s, out, st);
     default: return o ? launch_accum_w<4, true, true>(src, W, nblk, q, s, out, st)
                       : launch_accum_w<4, false, true>(src, W, nblk, q, s, out, st);
     }
