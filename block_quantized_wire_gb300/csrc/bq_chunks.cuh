@@ -510,6 +510,8 @@ int64_t chunks(int64_t nblk, int segs) { return (nblk + 2 * segs - 1) / (2 * seg
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool aligned32(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
 // Staged kernels keep STAGES bulk-copy slots per warp in dynamic shared memory.
 template <class Op, int STAGES, class Kernel, class... Args>
 cudaError_t launch_staged(Kernel kernel, int64_t nchunk, cudaStream_t st, Args... args)

@@ -117,6 +117,16 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void *p)
     return r;
 }
 
+// 32 bytes per lane in one 256-bit access: a warp reads or writes 1 KB of whole
+// sectors. The address must be 32-byte aligned; callers check the base pointer on the
+// host and take 16-byte accesses otherwise.
+__device__ __forceinline__ void ld_stream_v8(const void *p, uint4 &a, uint4 &b)
+{
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+        : "l"(p));
+}
+
 __device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
 {
     uint32_t r;
@@ -128,6 +138,13 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v8(void *p, uint4 a, uint4 b)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
                  : "memory");
 }
 

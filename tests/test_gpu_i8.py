@@ -247,6 +247,48 @@ def test_accumulate_repeated_source_and_tiny_sums():
         assert_same(sn, sa, "scales without owner output")
 
 
+def test_bf16_pointers_aligned_to_16_but_not_32_bytes():
+    # BF16 buffers need only 16-byte alignment; 32-byte-aligned ones take 256-bit
+    # accesses, the others 16-byte ones: both must give the same bytes
+    rng = np.random.default_rng(77)
+    nblk = 45
+    n = nblk * 128
+    xs = [adversarial_blocks(rng, nblk, max_abs=1.0e37).reshape(-1) for _ in range(4)]
+    for off in (0, 8):  # BF16 elements: 0 and 16 bytes past a 32-byte boundary
+        def bf16_at(bits_):
+            raw = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+            t = raw[off:off + n]
+            if bits_ is not None:
+                t.copy_(from_bits_bf16(bits_))
+            assert t.data_ptr() % 32 == 2 * off
+            return t
+        x = [bf16_at(b) for b in xs]
+        qs, ss = [], []
+        for w in range(4):
+            _, q, s_ = codec.empty_wire_i8(n)
+            codec.quant_i8(x[w], q, s_)
+            qr, sr = oracle.quant_i8(xs[w])
+            assert_same(q, qr, f"quant payload, offset {off}")
+            assert_same(s_, sr, f"quant scales, offset {off}")
+            qs.append(q)
+            ss.append(s_)
+        out = bf16_at(None)
+        codec.dequant_i8(qs[0], ss[0], out)
+        assert_same(out, oracle.dequant_i8(*oracle.quant_i8(xs[0])), f"materialize, offset {off}")
+        ref = [oracle.quant_i8(b) for b in xs]
+        _, qa, sa = codec.empty_wire_i8(n)
+        codec.dequant_accum_i8(qs, ss, qa, sa, out)
+        aq, as_, ao = oracle.dequant_accum_i8([r[0] for r in ref], [r[1] for r in ref], materialize=True)
+        assert_same(qa, aq, f"accumulate payload, offset {off}")
+        assert_same(out, ao, f"accumulate owner output, offset {off}")
+        _, qh, sh = codec.empty_wire_i8(n)
+        codec.ring_hop_i8(qs[0], ss[0], x[1], qh, sh, out)
+        hq, hs, ho = oracle.ring_hop_i8(ref[0][0], ref[0][1], xs[1], materialize=True)
+        assert_same(qh, hq, f"hop payload, offset {off}")
+        assert_same(sh, hs, f"hop scales, offset {off}")
+        assert_same(out, ho, f"hop owner output, offset {off}")
+
+
 def test_ring_hop_edge_cases():
     rng = np.random.default_rng(31)
     nblk = 200
