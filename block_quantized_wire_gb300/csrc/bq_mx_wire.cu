@@ -84,6 +84,208 @@ struct MxCodec {
     }
 };
 
+// ---------------------------------------------------------------- wide lanes
+// The layout of the block-INT8 wide kernels: a lane takes 16 consecutive values, so an
+// MX group spans 2 lanes and a 128-value block 8; a warp chunk is two 512-value
+// segments, 8 blocks, 32 groups: one per lane for the E8M0 computation. Same
+// arithmetic, same order.
+
+// Decode multiplier 2^(e-127) of the lane's group, from its block's scale word.
+__device__ __forceinline__ float mx_wide_mult(uint32_t word, int lane)
+{
+    const uint32_t e = (word >> (8 * ((lane & 7) >> 1))) & 0xffu;
+    return e == 255u ? __uint_as_float(0x7fc00000u) : exp2i(static_cast<int>(e) - 127);
+}
+
+// v[j][h]: the lane's values 8h..8h+7 of segment j (elements e0 + 512 j + 8 h ...), in
+// block b0 + 4 j + (lane >> 3), group ((lane & 7) >> 1) of that block. kV8: out is
+// 32-byte aligned and takes one 256-bit store per lane.
+template <bool kTail, bool kOut, bool kV8>
+__device__ __forceinline__ void requant_mx_wide(const float2 (&v)[2][2][4], int64_t e0, int64_t b0, int64_t nblk,
+                                                int lane, uint8_t *__restrict__ q, uint32_t *__restrict__ s,
+                                                uint16_t *__restrict__ out)
+{
+    const int g = lane >> 3;
+    float gmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        float m = fmaxf(amax8(v[j][0]), amax8(v[j][1]));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));  // the group's two lanes
+        // lane L takes chunk group L: segment L / 16, block (L / 4) % 4 of it, group L % 4
+        const float gm = __shfl_sync(kFull, m, 8 * ((lane >> 2) & 3) + 2 * (lane & 3));
+        if ((lane >> 4) == j) gmax = gm;
+    }
+    const uint32_t e = mx_scale_byte(gmax);
+    const float p = exp2i(127 - static_cast<int>(e));
+    const float pinv = exp2i(static_cast<int>(e) - 127);
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const int src = 16 * j + 4 * g + ((lane & 7) >> 1);
+        const float2 pj = splat(__shfl_sync(kFull, p, src));
+        const float pinv_j = kOut ? __shfl_sync(kFull, pinv, src) : 0.0f;
+        float2 y0[4], y1[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {  // exact: a power-of-two scaling
+            y0[i] = mul2(v[j][0][i], pj);
+            y1[i] = mul2(v[j][1][i], pj);
+        }
+        const uint2 c0 = f32x8_to_e4m3x8(y0), c1 = f32x8_to_e4m3x8(y1);
+        if (!kTail || b0 + 4 * j + g < nblk) {
+            st_v4(q + e0 + 512 * j, make_uint4(c0.x, c0.y, c1.x, c1.y));
+            if (kOut) {
+                float2 d0[4], d1[4];
+                e4m3x8_to_f32(c0, pinv_j, d0);
+                e4m3x8_to_f32(c1, pinv_j, d1);
+                const uint4 o0 = f32x8_to_bf16x8(d0), o1 = f32x8_to_bf16x8(d1);
+                if (kV8) {
+                    st_v8(out + e0 + 512 * j, o0, o1);
+                } else {
+                    st_v4(out + e0 + 512 * j, o0);
+                    st_v4(out + e0 + 512 * j + 8, o1);
+                }
+            }
+        }
+    }
+    uint32_t word = e << (8 * (lane & 3));
+    word |= __shfl_xor_sync(kFull, word, 1);
+    word |= __shfl_xor_sync(kFull, word, 2);
+    if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk)) s[b0 + (lane >> 2)] = word;
+}
+
+template <int W, bool kOut, bool kMore, bool kV8>
+struct AccumWideMx {
+    const MxSourceList &src;  // the kernel's __grid_constant__ parameter, read in place
+    int nsrc;
+    uint8_t *__restrict__ q;
+    uint32_t *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint4 q[W][2];
+        uint32_t sc[W];  // lanes 0..7: the scale words of the chunk's blocks 0..7
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load_group(In &in, int gsrc, int64_t c) const
+    {
+        const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
+        const int g = lane >> 3;
+        const bool lane_ok = lane < 8 && (!kTail || b0 + lane < nblk);
+#pragma unroll
+        for (int i = 0; i < W; i++) {
+            const bool src_ok = gsrc + i < nsrc;
+            const uint8_t *qw = src.q[src_ok ? gsrc + i : gsrc];
+            const uint32_t *sw = src.s[src_ok ? gsrc + i : gsrc];
+#pragma unroll
+            for (int j = 0; j < 2; j++)
+                in.q[i][j] = (src_ok && (!kTail || b0 + 4 * j + g < nblk)) ? ld_stream_v4(qw + e0 + 512 * j)
+                                                                           : make_uint4(0, 0, 0, 0);
+            in.sc[i] = (src_ok && lane_ok) ? ld_stream_u32(sw + b0 + lane) : 0u;
+        }
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        load_group<kTail>(in, 0, c);
+    }
+    template <bool kFirst>
+    __device__ __forceinline__ void add_group(const In &in, int gsrc, float2 (&acc)[2][2][4]) const
+    {
+        const int g = lane >> 3;
+#pragma unroll
+        for (int i = 0; i < W; i++) {
+            if (gsrc + i >= nsrc) break;
+#pragma unroll
+            for (int j = 0; j < 2; j++) {
+                const float mult = mx_wide_mult(__shfl_sync(kFull, in.sc[i], 4 * j + g), lane);
+                float2 d[2][4];
+                e4m3x8_to_f32(make_uint2(in.q[i][j].x, in.q[i][j].y), mult, d[0]);
+                e4m3x8_to_f32(make_uint2(in.q[i][j].z, in.q[i][j].w), mult, d[1]);
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) acc[j][h][e] = (kFirst && i == 0) ? d[h][e] : add2(acc[j][h][e], d[h][e]);
+            }
+        }
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float2 acc[2][2][4];
+        add_group<true>(in, 0, acc);
+        if constexpr (kMore) {
+            for (int gsrc = W; gsrc < nsrc; gsrc += W) {
+                In more;
+                load_group<kTail>(more, gsrc, c);
+                add_group<false>(more, gsrc, acc);
+            }
+        }
+        requant_mx_wide<kTail, kOut, kV8>(acc, c * 1024 + lane * 16, c * 8, nblk, lane, q, s, out);
+    }
+};
+
+template <bool kOut, bool kV8>
+struct HopWideMx {
+    const uint8_t *__restrict__ q_in;
+    const uint32_t *__restrict__ s_in;
+    const uint16_t *__restrict__ x;
+    uint8_t *__restrict__ q;
+    uint32_t *__restrict__ s;
+    uint16_t *__restrict__ out;
+    int64_t nblk;
+    int lane;
+    struct In {
+        uint4 q[2];
+        uint4 x[2][2];
+        uint32_t sc[2];  // the scale word of the lane's block, per segment
+    };
+    template <bool kTail>
+    __device__ __forceinline__ void load(In &in, int64_t c) const
+    {
+        const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8 + (lane >> 3);
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const bool ok = !kTail || b0 + 4 * j < nblk;
+            in.q[j] = ok ? ld_stream_v4(q_in + e0 + 512 * j) : make_uint4(0, 0, 0, 0);
+            if (!ok) {
+                in.x[j][0] = in.x[j][1] = make_uint4(0, 0, 0, 0);
+            } else if (kV8) {
+                ld_stream_v8(x + e0 + 512 * j, in.x[j][0], in.x[j][1]);
+            } else {
+                in.x[j][0] = ld_stream_v4(x + e0 + 512 * j);
+                in.x[j][1] = ld_stream_v4(x + e0 + 512 * j + 8);
+            }
+            in.sc[j] = ok ? ld_stream_u32(s_in + b0 + 4 * j) : 0u;
+        }
+    }
+    template <bool kTail>
+    __device__ __forceinline__ void compute(const In &in, int64_t c) const
+    {
+        float2 v[2][2][4];
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const float mult = mx_wide_mult(in.sc[j], lane);
+            float2 d[2][4], xl[2][4];
+            e4m3x8_to_f32(make_uint2(in.q[j].x, in.q[j].y), mult, d[0]);
+            e4m3x8_to_f32(make_uint2(in.q[j].z, in.q[j].w), mult, d[1]);
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                bf16x8_to_f32(in.x[j][h], xl[h]);
+#pragma unroll
+                for (int e = 0; e < 4; e++) v[j][h][e] = add2(d[h][e], xl[h][e]);
+            }
+        }
+        requant_mx_wide<kTail, kOut, kV8>(v, c * 1024 + lane * 16, c * 8, nblk, lane, q, s, out);
+    }
+};
+
+#ifndef BQ_MX_WIDE
+#define BQ_MX_WIDE 1
+#endif
+#ifndef BQ_HOP_MX_MIN_CTAS
+#define BQ_HOP_MX_MIN_CTAS 4
+#endif
+
 template <int SEGS, int W, bool kOut, bool kMore>
 using AccumMx = AccumOp<MxCodec, SEGS, W, kOut, kMore>;
 template <int SEGS, bool kOut>
@@ -137,6 +339,28 @@ ring_hop_mx_staged_kernel(const uint8_t *__restrict__ q_in, const uint32_t *__re
     run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<HopMx<SEGS, kOut>, STAGES>());
 }
 
+template <int W, bool kOut, bool kMore, bool kV8>
+__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MX_MIN_CTAS)
+accum_mx_wide_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t nblk, uint8_t *__restrict__ q,
+                     uint32_t *__restrict__ s, uint16_t *__restrict__ out)
+{
+    pdl_begin();
+    const AccumWideMx<W, kOut, kMore, kV8> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 8);
+}
+
+template <bool kOut, bool kV8>
+__global__ void __launch_bounds__(kThreads, BQ_HOP_MX_MIN_CTAS)
+ring_hop_mx_wide_kernel(const uint8_t *__restrict__ q_in, const uint32_t *__restrict__ s_in,
+                        const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ q,
+                        uint32_t *__restrict__ s, uint16_t *__restrict__ out)
+{
+    pdl_begin();
+    const HopWideMx<kOut, kV8> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
+    run_chunks<false>(op, nblk, 8);
+}
+
+
 // Segments per warp chunk and bulk-copy stages per warp (0: direct global loads).
 #ifndef BQ_SEGS_ACCUM_MX
 #define BQ_SEGS_ACCUM_MX 4
@@ -154,6 +378,16 @@ constexpr int kSegsAccumMx = BQ_SEGS_ACCUM_MX;
 constexpr int kSegsHopMx = BQ_SEGS_HOP_MX;
 constexpr int kStagesAccumMx = BQ_STAGES_ACCUM_MX;
 constexpr int kStagesHopMx = BQ_STAGES_HOP_MX;
+
+template <int W, bool kMore>
+cudaError_t launch_accum_mx_wide(const MxSourceList &src, int nsrc, int64_t nblk, uint8_t *q, uint32_t *s,
+                                 uint16_t *out, bool o, bool v8, cudaStream_t st)
+{
+    auto kernel = o ? (v8 ? accum_mx_wide_kernel<W, true, kMore, true> : accum_mx_wide_kernel<W, true, kMore, false>)
+                    : accum_mx_wide_kernel<W, false, kMore, false>;
+    BQK_GRID(kernel, chunks(nblk, 4));
+    return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
+}
 
 template <int W, bool kOut, bool kMore>
 cudaError_t launch_accum_mx_w(const MxSourceList &src, int nsrc, int64_t nblk, uint8_t *q, uint32_t *s,
@@ -194,6 +428,16 @@ cudaError_t launch_hop_mx_stages(const uint8_t *q_in, const uint32_t *s_in, cons
 cudaError_t launch_accum_mx(const MxSourceList &src, int W, int64_t nblk, uint8_t *q, uint32_t *s, uint16_t *out,
                             cudaStream_t st)
 {
+    if (BQ_MX_WIDE) {
+        const bool o = out != nullptr, v8 = o && aligned32(out);
+        switch (W) {
+        case 1: return launch_accum_mx_wide<1, false>(src, W, nblk, q, s, out, o, v8, st);
+        case 2: return launch_accum_mx_wide<2, false>(src, W, nblk, q, s, out, o, v8, st);
+        case 3: return launch_accum_mx_wide<3, false>(src, W, nblk, q, s, out, o, v8, st);
+        case 4: return launch_accum_mx_wide<4, false>(src, W, nblk, q, s, out, o, v8, st);
+        default: return launch_accum_mx_wide<4, true>(src, W, nblk, q, s, out, o, v8, st);
+        }
+    }
     const bool o = out != nullptr;
     switch (W) {
     case 1: return o ? launch_accum_mx_w<1, true, true>(src, W, nblk, q, s, out, st)
@@ -210,6 +454,13 @@ cudaError_t launch_accum_mx(const MxSourceList &src, int W, int64_t nblk, uint8_
 cudaError_t launch_ring_hop_mx(const uint8_t *q_in, const uint32_t *s_in, const uint16_t *x, int64_t nblk, uint8_t *q,
                                uint32_t *s, uint16_t *out, cudaStream_t st)
 {
+    if (BQ_MX_WIDE) {
+        const bool v8 = aligned32(x) && (!out || aligned32(out));
+        auto kernel = out ? (v8 ? ring_hop_mx_wide_kernel<true, true> : ring_hop_mx_wide_kernel<true, false>)
+                          : (v8 ? ring_hop_mx_wide_kernel<false, true> : ring_hop_mx_wide_kernel<false, false>);
+        BQK_GRID(kernel, chunks(nblk, 4));
+        return launch_kernel(kernel, grid, st, q_in, s_in, x, nblk, q, s, out);
+    }
     if (out) return launch_hop_mx_stages<kStagesHopMx, true>(q_in, s_in, x, nblk, q, s, out, st);
     return launch_hop_mx_stages<kStagesHopMx, false>(q_in, s_in, x, nblk, q, s, nullptr, st);
 }

@@ -165,18 +165,47 @@ def test_mx_ragged_sizes(nblk):
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 7, 8, 9, 16])
-def test_mx_accumulate_any_width(W):
-    rng = np.random.default_rng(600 + W)
-    nblk = 37
+@pytest.mark.parametrize("owner", [True, False])
+@pytest.mark.parametrize("nblk", [37, 8, 1])
+def test_mx_accumulate_any_width(W, owner, nblk):
+    # with and without the owner output, whole and partial chunks
+    rng = np.random.default_rng(600 + W + nblk)
     qs, ss = random_wires(rng, W, nblk, e_lo=60, e_hi=200)
     n = nblk * 128
     _, qo, so = codec.empty_wire_mx(n)
     out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
-    codec.dequant_accum_mx([dev(q) for q in qs], [dev(s) for s in ss], qo, so, out)
+    codec.dequant_accum_mx([dev(q) for q in qs], [dev(s) for s in ss], qo, so, out if owner else None)
     qa, sa, oa = oracle.dequant_accum_mx(qs, ss, materialize=True)
     assert_same(qo, qa, "codes")
     assert_same(so, sa, "scales")
-    assert_same(out, oa, "materialized")
+    if owner:
+        assert_same(out, oa, "materialized")
+
+
+def test_mx_bf16_pointers_aligned_to_16_but_not_32_bytes():
+    # the wide kernels take 256-bit BF16 accesses only at 32-byte-aligned pointers
+    rng = np.random.default_rng(702)
+    nblk, W = 45, 4
+    qs, ss = random_wires(rng, W, nblk, e_lo=60, e_hi=200)
+    n = nblk * 128
+    x_loc = adversarial_blocks(rng, nblk, max_abs=1.0e37).reshape(-1)
+    for off in (0, 8):  # BF16 elements: 0 and 16 bytes past a 32-byte boundary
+        raw_out = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+        out = raw_out[off:off + n]
+        raw_x = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+        x = raw_x[off:off + n]
+        x.copy_(from_bits_bf16(x_loc))
+        assert out.data_ptr() % 32 == 2 * off and x.data_ptr() % 32 == 2 * off
+        _, qo, so = codec.empty_wire_mx(n)
+        codec.dequant_accum_mx([dev(q) for q in qs], [dev(s) for s in ss], qo, so, out)
+        qa, sa, oa = oracle.dequant_accum_mx(qs, ss, materialize=True)
+        assert_same(qo, qa, f"accumulated codes, offset {off}")
+        assert_same(out, oa, f"accumulate owner output, offset {off}")
+        codec.ring_hop_mx(dev(qs[1]), dev(ss[1]), x, qo, so, out)
+        qh, sh, oh = oracle.ring_hop_mx(qs[1], ss[1], x_loc, materialize=True)
+        assert_same(qo, qh, f"hop codes, offset {off}")
+        assert_same(so, sh, f"hop scales, offset {off}")
+        assert_same(out, oh, f"hop owner output, offset {off}")
 
 
 def test_mx_accumulate_tiny_and_cancelling_sums():
