@@ -6,6 +6,7 @@ raises. Build it with ``block_quantized_wire_gb300.build.build_library()`` (or
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -59,24 +60,44 @@ def library_path() -> str:
     return _build.LIB
 
 
+def _open(path: str):
+    if not os.path.exists(path):
+        raise ImportError(f"{os.path.basename(path)} is not built ({path}); run "
+                          "block_quantized_wire_gb300.build.build_library()")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _PROTOS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if lib.bq_abi_version() != ABI_VERSION:
+        raise ImportError(f"{path}: ABI version {lib.bq_abi_version()} != {ABI_VERSION}")
+    return lib
+
+
 def load():
     """Load libbq.so once; raise if it is not built or does not load."""
     global _lib
     with _lock:
         if _lib is None:
-            path = library_path()
-            if not os.path.exists(path):
-                raise ImportError(
-                    f"libbq.so is not built ({path}); run block_quantized_wire_gb300.build.build_library()")
-            lib = ctypes.CDLL(path)
-            for name, (args, res) in _PROTOS.items():
-                fn = getattr(lib, name)
-                fn.argtypes = args
-                fn.restype = res
-            if lib.bq_abi_version() != ABI_VERSION:
-                raise ImportError(f"libbq.so ABI version {lib.bq_abi_version()} != {ABI_VERSION}")
-            _lib = lib
+            _lib = _open(library_path())
     return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every call of this package to another build of the same sources (the
+    tests run the compile-time alternatives of the kernels through it). Not for
+    concurrent use with other calls."""
+    global _lib
+    alt = _open(path)
+    with _lock:
+        saved = _lib
+        _lib = alt
+    try:
+        yield alt
+    finally:
+        with _lock:
+            _lib = saved
 
 
 def check(func: str, status: int) -> None:

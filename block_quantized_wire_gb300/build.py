@@ -20,6 +20,12 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libbq.so")
 OBJDIR = os.path.join(PKG, "_build")
+# The same sources with the compile-time alternatives of the measured defaults: the
+# 8-value-per-lane quantize, accumulate and ring hop, the bulk-copy-staged hops, no
+# 256-bit accesses. Tests build it to keep those paths bit-exact too.
+ALT_LIB = os.path.join(PKG, "libbq_alt.so")
+ALT_OBJDIR = os.path.join(PKG, "_build_alt")
+ALT_FLAGS = ["-DBQ_ACCUM_WIDE=0", "-DBQ_QUANT_WIDE=0", "-DBQ_HOP_WIDE=0", "-DBQ_MX_WIDE=0", "-DBQ_WIDE_V8=0"]
 
 SOURCES = ["bq_api.cu", "bq_i8.cu", "bq_mx.cu", "bq_mx_wire.cu", "bq_e4m3.cu"]
 HEADERS = ["bq_device.cuh", "bq_launch.h", "bq_chunks.cuh"]
@@ -43,37 +49,43 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build_library(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libbq.so if any source is newer than it; returns its path.
+def build_library(force: bool = False, verbose: bool = False, extra_flags=(), lib: str = LIB,
+                  objdir: str = OBJDIR) -> str:
+    """Compile and link `lib` (libbq.so) if any source is newer than it; returns its path.
 
     Concurrent callers (one process per GPU under torchrun) are serialized by a file
     lock: the first builds, the others find the library up to date. The library is
     replaced atomically, so a process that already loaded it is unaffected."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
-    with open(os.path.join(OBJDIR, ".lock"), "w") as lock:
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
+    with open(os.path.join(objdir, ".lock"), "w") as lock:
         fcntl.flock(lock, fcntl.LOCK_EX)
         try:
-            if not force and up_to_date():
-                return LIB
-            return _build_locked(verbose, extra_flags)
+            if not force and up_to_date(lib):
+                return lib
+            return _build_locked(verbose, extra_flags, lib, objdir)
         finally:
             fcntl.flock(lock, fcntl.LOCK_UN)
 
 
-def _build_locked(verbose: bool, extra_flags) -> str:
+def build_alt_library(force: bool = False, verbose: bool = False) -> str:
+    """Build libbq_alt.so: the sources with ALT_FLAGS."""
+    return build_library(force, verbose, ALT_FLAGS, ALT_LIB, ALT_OBJDIR)
+
+
+def _build_locked(verbose: bool, extra_flags, lib: str, objdir: str) -> str:
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c",
                os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -85,13 +97,13 @@ def _build_locked(verbose: bool, extra_flags) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".%d.tmp" % os.getpid()
+    tmp = lib + ".%d.tmp" % os.getpid()
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -294,3 +294,16 @@ def test_binding_rejects_tensors_on_another_device(monkeypatch):
     with pytest.raises(ValueError, match="current CUDA device"):
         codec.quant_i8(x0, q1, s, stream=0)
     assert not called
+
+
+def test_use_library_routes_calls_and_restores_the_default(bq_lib):
+    from block_quantized_wire_gb300 import _lib, build
+    main = _lib.load()
+    with _lib.use_library(build.LIB) as other:
+        assert _lib.load() is other and other is not main
+        assert other.bq_abi_version() == _lib.ABI_VERSION
+    assert _lib.load() is main
+    with pytest.raises(ImportError):
+        with _lib.use_library(os.path.join(os.path.dirname(build.LIB), "no_such_library.so")):
+            pass
+    assert _lib.load() is main

@@ -101,11 +101,13 @@ def test_error_vs_unquantized_sum_is_within_half_step_bounds():
 
 
 def test_bounded_waits_do_not_run_out_and_can_be_observed():
-    # the staged kernels ran throughout the suite without an abandoned wait
+    # kernels that stage their inputs through bulk copies (the ring hops of the
+    # alternative build, which also runs this test) leave no abandoned wait
     codec.take_wait_timeouts()  # clear whatever earlier tests left
     xs = [x.cuda() for x in inputs.a2a_3072(rows=3072)]
     topology.i8_a2a(xs)
-    topology.mx_ring(xs)  # the MX hop stages its inputs too (its own counter)
+    topology.i8_ring(xs)
+    topology.mx_ring(xs)
     torch.cuda.synchronize()
     assert codec.take_wait_timeouts() == 0
     # a wait that nothing completes gives up after its limit and is counted; the
