@@ -166,6 +166,25 @@ def test_e4m3_ragged_and_adversarial(nblk):
     assert gq.bands_intact() and gs.bands_intact() and go.bands_intact()
 
 
+def test_e4m3_input_aligned_to_16_but_not_32_bytes():
+    # 32-byte-aligned BF16 input takes 256-bit loads, other 16-byte-aligned input two
+    # 16-byte loads: the same codes and scales
+    rng = np.random.default_rng(91)
+    nblk = 45
+    xb = adversarial_blocks(rng, nblk).reshape(-1)
+    n = xb.size
+    qr, sr = oracle.quant_e4m3(xb)
+    for off in (0, 8):
+        raw = torch.empty(n + 16, dtype=torch.bfloat16, device="cuda")
+        x = raw[off:off + n]
+        x.copy_(from_bits_bf16(xb))
+        assert x.data_ptr() % 32 == 2 * off
+        _, q, s = codec.empty_wire_e4m3(n)
+        codec.quant_e4m3(x, q, s)
+        assert_same(q, qr, f"codes, offset {off}")
+        assert_same(s, sr, f"scales, offset {off}")
+
+
 def test_e4m3_scales_across_the_exact_division_cutoff():
     # s = amax / 448 >= 2^-90 exactly when amax >= 448 * 2^-90 = 2^-81.19, BF16 bits
     # 0x16e0 and up: every BF16 amax from 0x1600 to 0x1700 straddles the cutoff between
