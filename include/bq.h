@@ -266,10 +266,12 @@ BQ_API bq_status bq_reduce_quant_e4m3(const void *const *x_srcs, int W, int64_t 
                                float *scales, void *out_bf16, cudaStream_t stream);
 
 /* Number of bounded waits inside codec kernels that ran out since the previous call;
- * the count is reset to 0. Kernels that stage their inputs through shared memory wait
- * on hardware bulk-copy completions. A wait that has not completed within 1 s is
- * abandoned: that warp stops early (the outputs of the chunks it had not reached are
- * not written) and this count grows by one, instead of the kernel spinning forever.
+ * the count is reset to 0. Kernels that stage their inputs through shared memory (the
+ * bulk-copy ring hops, a build-time alternative; the default kernels load directly and
+ * wait on nothing) wait on hardware bulk-copy completions. A wait that has not
+ * completed within 1 s is abandoned: that warp stops early (the outputs of the chunks
+ * it had not reached are not written) and this count grows by one, instead of the
+ * kernel spinning forever.
  * Synchronizes with the current device (the count lives in device memory).
  *   count  host pointer receiving the number of abandoned waits. */
 BQ_API bq_status bq_take_wait_timeouts(int64_t *count);
