@@ -389,6 +389,29 @@ __device__ __forceinline__ float amax8(const float2 (&v)[4])
     return m;
 }
 
+// max(a, b, c) in one instruction (three-input max of sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+#ifndef BQ_MAX3
+#define BQ_MAX3 1
+#endif
+// max |x| over a lane's 16 values (a: values 0..7, b: values 8..15)
+__device__ __forceinline__ float amax16(const float2 (&a)[4], const float2 (&b)[4])
+{
+    if (!BQ_MAX3) return fmaxf(amax8(a), amax8(b));
+    const float m0 = max3f(fabsf(a[0].x), fabsf(a[0].y), fabsf(a[1].x));
+    const float m1 = max3f(fabsf(a[1].y), fabsf(a[2].x), fabsf(a[2].y));
+    const float m2 = max3f(fabsf(a[3].x), fabsf(a[3].y), fabsf(b[0].x));
+    const float m3 = max3f(fabsf(b[0].y), fabsf(b[1].x), fabsf(b[1].y));
+    const float m4 = max3f(fabsf(b[2].x), fabsf(b[2].y), fabsf(b[3].x));
+    return fmaxf(max3f(m0, m1, m2), max3f(m3, m4, fabsf(b[3].y)));
+}
+
 // max over the 16 lanes of a half-warp (xor partners stay inside the half)
 __device__ __forceinline__ float halfwarp_max(float m)
 {

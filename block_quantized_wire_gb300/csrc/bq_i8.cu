@@ -176,7 +176,7 @@ __device__ __forceinline__ void requant_wide(const float2 (&v)[2][2][4], int64_t
     const int g = lane >> 3;
     float m[2];
 #pragma unroll
-    for (int j = 0; j < 2; j++) m[j] = octet_max(fmaxf(amax8(v[j][0]), amax8(v[j][1])));
+    for (int j = 0; j < 2; j++) m[j] = octet_max(amax16(v[j][0], v[j][1]));
     // lane b < 8 computes the scale of the chunk's block b: segment b / 4, lane group b % 4
     float mine = 0.0f;
 #pragma unroll

@@ -109,7 +109,7 @@ __device__ __forceinline__ void requant_mx_wide(const float2 (&v)[2][2][4], int6
     float gmax = 0.0f;
 #pragma unroll
     for (int j = 0; j < 2; j++) {
-        float m = fmaxf(amax8(v[j][0]), amax8(v[j][1]));
+        float m = amax16(v[j][0], v[j][1]);
         m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));  // the group's two lanes
         // lane L takes chunk group L: segment L / 16, block (L / 4) % 4 of it, group L % 4
         const float gm = __shfl_sync(kFull, m, 8 * ((lane >> 2) & 3) + 2 * (lane & 3));
