@@ -307,3 +307,13 @@ def test_use_library_routes_calls_and_restores_the_default(bq_lib):
         with _lib.use_library(os.path.join(os.path.dirname(build.LIB), "no_such_library.so")):
             pass
     assert _lib.load() is main
+
+
+def test_alternative_build_flags_name_existing_switches():
+    # a misspelt switch would build the defaults again under the alternative's name
+    from block_quantized_wire_gb300 import build
+    src = "".join(open(os.path.join(build.CSRC, f)).read() for f in build.SOURCES + build.HEADERS)
+    for flag in build.ALT_FLAGS:
+        m = re.fullmatch(r"-D(BQ_[A-Z0-9_]+)=0", flag)
+        assert m, flag
+        assert f"#ifndef {m.group(1)}" in src and f"#define {m.group(1)} 1" in src, flag
