@@ -33,7 +33,9 @@ def test_alt_int8_kernels(alt):
         t8.test_accumulate_repeated_source_and_tiny_sums()
         t8.test_near_half_quotients_take_exact_path()
         t8.test_tiny_scale_blocks_across_the_exact_division_cutoff()
-        t8.test_ring_hop_edge_cases()
+        for nblk in (200, 45):
+            for owner in (True, False):
+                t8.test_ring_hop_edge_cases(nblk, owner)
         t8.test_accumulate_with_scales_not_16_byte_aligned()
         t8.test_ring_hop_with_scales_not_16_byte_aligned()
         t8.test_bf16_pointers_aligned_to_16_but_not_32_bytes()

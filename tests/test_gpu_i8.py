@@ -289,9 +289,11 @@ def test_bf16_pointers_aligned_to_16_but_not_32_bytes():
         assert_same(out, ho, f"hop owner output, offset {off}")
 
 
-def test_ring_hop_edge_cases():
+@pytest.mark.parametrize("owner", [True, False])
+@pytest.mark.parametrize("nblk", [200, 45])
+def test_ring_hop_edge_cases(nblk, owner):
+    # whole and partial last chunks, with and without the owner output
     rng = np.random.default_rng(31)
-    nblk = 200
     x_in = adversarial_blocks(rng, nblk, max_abs=1.0e38).reshape(-1)
     x_loc = adversarial_blocks(rng, nblk, max_abs=1.0e38).reshape(-1)
     x_loc[:128 * 9] = x_in[:128 * 9] ^ 0x8000  # blocks where the hop cancels to tiny sums
@@ -299,12 +301,15 @@ def test_ring_hop_edge_cases():
     n = x_in.size
     gq, gs, go = Guarded(n), Guarded(4 * nblk), Guarded(2 * n)
     codec.ring_hop_i8(torch.from_numpy(q_in).cuda(), torch.from_numpy(s_in).cuda(), from_bits_bf16(x_loc),
-                      gq.view(torch.int8), gs.view(torch.float32), go.view(torch.bfloat16))
+                      gq.view(torch.int8), gs.view(torch.float32), go.view(torch.bfloat16) if owner else None)
     qh, sh, oh = oracle.ring_hop_i8(q_in, s_in, x_loc, materialize=True)
     assert np.all(np.isfinite(sh))
     assert_same(gq.view(torch.int8), qh, "payload")
     assert_same(gs.view(torch.float32), sh, "scales")
-    assert_same(go.view(torch.bfloat16), oh, "materialized")
+    if owner:
+        assert_same(go.view(torch.bfloat16), oh, "materialized")
+    else:
+        assert (go.raw == Guarded.SENTINEL).all().item()  # no owner output: nothing written
     assert gq.bands_intact() and gs.bands_intact() and go.bands_intact()
 
 
