@@ -195,8 +195,8 @@ def quant_mx_tiled(x: torch.Tensor, q: torch.Tensor, s_tiled: torch.Tensor, g_to
                    stream=None) -> None:
     """BF16 or FP16 x [rows, cols] -> E4M3 q [rows, cols] and E8M0 scales written into the
     tiled GEMM layout of a tensor with g_total scale columns, starting at scale column g0
-    (the slice's column offset / 32). Parity of the layout itself is unpinned: the pages
-    do not print it (include/bq.h, bq_quant_mx_tiled)."""
+    (the slice's column offset / 32). The pages do not print the layout; it is the
+    block-scaled GEMM operand layout described in include/bq.h (bq_quant_mx_tiled)."""
     f16 = x.dtype == torch.float16
     xp, rows, cols, ld_x = _rows(x, torch.float16 if f16 else torch.bfloat16, "x")
     qp, qr, qc, ld_q = _rows(q, torch.uint8, "q")
@@ -314,10 +314,18 @@ def reduce_quant_e4m3(x_srcs: Sequence[torch.Tensor], q: torch.Tensor, scales: t
 
 # ---------------------------------------------------------------- bounded waits
 def take_wait_timeouts() -> int:
-    """Waits inside codec kernels that ran out (1 s limit) since the last call; resets the
-    count. Synchronizes with the device."""
+    """Waits inside codec kernels on the current device that ran out (1 s limit) since
+    the previous call. Synchronizes with the device."""
     n = ctypes.c_int64(0)
     check("bq_take_wait_timeouts", load().bq_take_wait_timeouts(ctypes.byref(n)))
+    return int(n.value)
+
+
+def take_wait_unlanded() -> int:
+    """Bulk copies that had not landed within the limit after an abandoned wait, since
+    the previous call (each may have written a finished block's shared memory)."""
+    n = ctypes.c_int64(0)
+    check("bq_take_wait_unlanded", load().bq_take_wait_unlanded(ctypes.byref(n)))
     return int(n.value)
 
 

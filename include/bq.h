@@ -96,7 +96,7 @@ extern "C" {
 #define BQ_API
 #endif
 
-#define BQ_ABI_VERSION 4
+#define BQ_ABI_VERSION 5
 #define BQ_BLOCK_I8 128 /* values per INT8 block */
 #define BQ_GROUP_MX 32  /* values per E8M0 scale */
 #define BQ_MAX_W 16     /* most sources one accumulate call takes */
@@ -218,8 +218,9 @@ BQ_API bq_status bq_quant_mx_f16(const void *x_f16, int64_t rows, int64_t cols, 
 /* bq_quant_mx (BF16, or FP16 when x_is_f16 != 0) writing the E8M0 scales in the tiled
  * layout that block-scaled GEMM operands use, for a GEMM that consumes the assembled
  * MXFP8 input ("[II] Support staged MXFP8 linear inputs", Behavior: empty_input
- * allocates values and scale layouts; mm_quantized runs the GEMM on them). PARITY
- * UNPINNED: the pages do not print this layout; it is the publicly described one:
+ * allocates values and scale layouts; mm_quantized runs the GEMM on them). The pages
+ * do not print this layout; it is the publicly described one that cuBLAS block-scaled
+ * GEMMs read ("1D block scaling factors layout"), the same as PyTorch's to_blocked:
  * the scale matrix S [rows_total, g_total] (g_total = columns of the whole tensor / 32,
  * a multiple of 4) is cut into tiles of 128 rows x 4 scale columns, tile (R, C) stored
  * as 512 bytes at (R * g_total/4 + C) * 512, and inside a tile row r, column c at byte
@@ -265,16 +266,27 @@ BQ_API bq_status bq_dequant_e4m3(const uint8_t *q, const float *scales, int64_t 
 BQ_API bq_status bq_reduce_quant_e4m3(const void *const *x_srcs, int W, int64_t n, uint8_t *q,
                                float *scales, void *out_bf16, cudaStream_t stream);
 
-/* Number of bounded waits inside codec kernels that ran out since the previous call;
- * the count is reset to 0. Kernels that stage their inputs through shared memory (the
- * bulk-copy ring hops, a build-time alternative; the default kernels load directly and
- * wait on nothing) wait on hardware bulk-copy completions. A wait that has not
- * completed within 1 s is abandoned: that warp stops early (the outputs of the chunks
- * it had not reached are not written) and this count grows by one, instead of the
- * kernel spinning forever.
- * Synchronizes with the current device (the count lives in device memory).
- *   count  host pointer receiving the number of abandoned waits. */
+/* Number of bounded waits inside codec kernels on the current device that ran out
+ * since the previous call of this function there (the first call counts from library
+ * load). Kernels that stage their inputs through shared memory (the bulk-copy ring
+ * hops, a build-time alternative; the default kernels load directly and wait on
+ * nothing) wait on hardware bulk-copy completions. A wait that has not completed
+ * within 1 s is abandoned: that warp stops early (the outputs of the chunks it had not
+ * reached are not written) and this count grows by one, instead of the kernel spinning
+ * forever. The device-side counters are never reset, so a timeout that happens during
+ * this call is reported by the next one, never lost.
+ * Synchronizes with the current device (the counters live in device memory).
+ *   count  host pointer receiving the number of abandoned waits
+ * Returns BQ_ERR_CUDA if a counter cannot be read; nothing is consumed then. */
 BQ_API bq_status bq_take_wait_timeouts(int64_t *count);
+
+/* After an abandoned wait the warp gives its copies still in flight time to land, each
+ * wait again bounded by 1 s, before its block exits. This is the number of such drain
+ * waits that ran out too, since the previous call on the current device: each means a
+ * bulk copy may have written that block's shared memory after the block exited. It is
+ * 0 unless bq_take_wait_timeouts reported a timeout. Same conventions as
+ * bq_take_wait_timeouts. */
+BQ_API bq_status bq_take_wait_unlanded(int64_t *count);
 
 /* Self-test of the bounded wait: one warp waits on a barrier that nothing completes,
  * with a 20 ms limit, so the count read by bq_take_wait_timeouts grows by exactly one.

@@ -27,8 +27,10 @@ Each function follows the pull-request pages on the wire codec:
   page, Summary.
 * ``quant_e4m3`` / ``dequant_e4m3``: the legacy E4M3 codec the block-INT8 page
   compares against (Summary and Why: one E4M3 byte per value, FP32 scale per 128).
-* ``mx_scales_to_tiled``: the tiled E8M0 layout block-scaled GEMMs read. PARITY
-  UNPINNED: the staged-input page names scale layouts for its GEMM but prints none.
+* ``mx_scales_to_tiled``: the tiled E8M0 layout block-scaled GEMMs read. The
+  staged-input page names scale layouts for its GEMM but prints none; the tests pin
+  this one to PyTorch's independent statements of cuBLAS's block-scaling-factor
+  layout (``to_blocked`` / ``from_blocked``).
 """
 from __future__ import annotations
 

@@ -540,11 +540,13 @@ int bqo_reduce_quant_e4m3(const uint16_t *const *x_srcs, int W, int64_t n, uint8
 
 /* ------------------------------------------------------------------------ */
 /* Tiled E8M0 scale layout for block-scaled GEMM operands.                   */
-/* PARITY UNPINNED: the staged-input page mentions scale layouts for the    */
-/* GEMM ("[II] Support staged MXFP8 linear inputs", Behavior: empty_input    */
-/* allocates MXFP8 values and scale layouts) but prints none. This is the   */
-/* tiled layout that Blackwell block-scaled matrix multiplies read, stated  */
-/* from its public description; nothing on the pages can confirm it.        */
+/* The staged-input page mentions scale layouts for the GEMM ("[II] Support */
+/* staged MXFP8 linear inputs", Behavior: empty_input allocates MXFP8       */
+/* values and scale layouts) but prints none. This is the tiled layout that */
+/* Blackwell block-scaled matrix multiplies read (cuBLAS, "1D block scaling */
+/* factors layout"), stated from its public description. The tests pin it   */
+/* to PyTorch's independent statements of that layout (to_blocked and       */
+/* from_blocked in torch's quantized-test helpers) element by element.      */
 /*                                                                          */
 /* The scale matrix S [rows, g] (g = cols/32) is cut into tiles of 128 rows */
 /* by 4 scale columns; tile (R, C) holds rows 128R..128R+127 and columns    */

@@ -258,7 +258,7 @@ def test_mx_f16_every_value_and_ragged_rows():
     assert_same(s2, sr2, "scales")
 
 
-# ------------------------------------------------------------------ tiled scale layout (parity unpinned vs the pages)
+# ------------------------------------------------------------------ tiled scale layout (pinned on the CPU to torch's to_blocked)
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_mx_tiled_scales_staged_slices(dtype):
     # six staged slices of 300 rows (a ragged last tile row) into one tiled scale buffer;
@@ -282,3 +282,48 @@ def test_mx_tiled_scales_staged_slices(dtype):
     assert_same(q, qr, "codes")
     want = oracle.mx_scales_to_tiled(sr, fill=0xA5)
     assert_same(tiled, want, "tiled scales")
+
+
+def test_mx_tiled_scales_feed_a_block_scaled_gemm():
+    # The layout's consumer: a block-scaled MXFP8 GEMM (PyTorch's _scaled_mm with E8M0
+    # scales, cuBLASLt underneath) reads E4M3 codes and tiled scales that this library
+    # wrote, A staged from two slices at scale-column offsets 0 and 8. Its result must
+    # equal the float64 product of the two operands' materializations up to the GEMM's
+    # FP32 accumulation and its BF16 output rounding; a misplaced scale would scale
+    # whole 32-value groups by powers of two and miss by far more.
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("this torch has no float8_e8m0fnu")
+    M, N, K = 256, 256, 512
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    a = torch.randn((M, K), generator=g, device="cuda").to(torch.bfloat16)
+    b = (torch.randn((N, K), generator=g, device="cuda") * 3).to(torch.bfloat16)
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    qb = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sa = torch.zeros((codec.mx_tiled_scale_bytes(M, K // 32),), dtype=torch.uint8, device="cuda")
+    sb = torch.zeros((codec.mx_tiled_scale_bytes(N, K // 32),), dtype=torch.uint8, device="cuda")
+    for c0 in (0, K // 2):
+        codec.quant_mx_tiled(a[:, c0:c0 + K // 2], qa[:, c0:c0 + K // 2], sa, K // 32, c0 // 32)
+    codec.quant_mx_tiled(b, qb, sb, K // 32, 0)
+    try:
+        c = torch._scaled_mm(qa.view(torch.float8_e4m3fn), qb.view(torch.float8_e4m3fn).t(),
+                             sa.view(torch.float8_e8m0fnu), sb.view(torch.float8_e8m0fnu), out_dtype=torch.bfloat16)
+    except (RuntimeError, TypeError, ValueError, NotImplementedError) as e:
+        pytest.skip(f"no MXFP8 block-scaled GEMM in this torch/cuBLAS on this GPU: {str(e).splitlines()[0][:160]}")
+    torch.cuda.synchronize()
+    # the operands' values: row-major scales from the same kernel body, materialized
+    qr, sr = codec.empty_mx(M, K)
+    qc, sc = codec.empty_mx(N, K)
+    codec.quant_mx(a, qr, sr)
+    codec.quant_mx(b, qc, sc)
+    assert torch.equal(qr, qa) and torch.equal(qc, qb)
+    da = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    db = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    codec.dequant_mx(qr, sr, da)
+    codec.dequant_mx(qc, sc, db)
+    ref = da.double() @ db.double().t()
+    mag = da.double().abs() @ db.double().abs().t()
+    err = (c.double() - ref).abs()
+    bound = ref.abs() * 2.0 ** -8 + mag * K * 2.0 ** -23 + 1e-30
+    assert bool((err <= bound).all()), f"max err {err.max().item()}, worst ratio {(err / bound).max().item()}"
+    assert err.max().item() < 0.05 * ref.abs().max().item()

@@ -793,26 +793,74 @@ def test_mx_f16_staged_slices_equal_concatenated():
 
 
 # ------------------------------------------------------------------ tiled scale layout
-def test_mx_tiled_scale_layout_is_a_tile_wise_bijection():
-    # PARITY UNPINNED against the pages (they print no GEMM scale layout); these checks
-    # only confirm that the oracle's layout is the stated one: every scale lands in its
-    # own byte, each 128 x 4 tile is one contiguous 512-byte run in row-tile-major order,
-    # and inside a tile each 16-byte line holds rows r, r+32, r+64, r+96.
-    rows, g = 256, 12
-    seen = {}
-    for r in range(rows):
-        for c in range(g):
-            off = oracle.mx_tiled_scale_offset(r, c, g)
-            assert off not in seen
-            seen[off] = (r, c)
-            tile = off // 512
-            assert tile == (r // 128) * (g // 4) + c // 4
-            within = off % 512
-            assert within // 16 == r % 32 and (within % 16) // 4 == (r % 128) // 32 and within % 4 == c % 4
-    assert sorted(seen) == list(range(oracle.mx_tiled_scale_bytes(rows, g)))
-    s = np.arange(rows * g, dtype=np.uint32).astype(np.uint8).reshape(rows, g)
-    t = oracle.mx_scales_to_tiled(s)
-    assert all(t[off] == s[r, c] for off, (r, c) in seen.items())
+# The staged-input page ("[II] Support staged MXFP8 linear inputs", Behavior) has
+# empty_input allocate "MXFP8 values and scale layouts" for its GEMM but prints no
+# layout. The oracle's tiled layout is pinned to an independent statement of the
+# layout that Blackwell block-scaled GEMMs read: PyTorch's own test helpers
+# `to_blocked` (tile rearrangement by reshapes, citing cuBLAS's "1D block scaling
+# factors layout") and `from_blocked` (the per-element offset formula of the same
+# cuBLAS section, written as loops). They live in a torch test module whose import
+# needs test-only packages, so the two functions are parsed out of the installed file
+# and executed on their own; nothing of them is copied here.
+def _torch_block_layout():
+    import ast
+    path = os.path.join(os.path.dirname(torch.__file__), "testing", "_internal", "common_quantized.py")
+    if not os.path.exists(path):
+        pytest.skip("this torch build does not ship common_quantized.py")
+    tree = ast.parse(open(path).read(), path)
+    want = {"ceil_div", "to_blocked", "from_blocked"}
+    funcs = [n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name in want]
+    if {f.name for f in funcs} != want:
+        pytest.skip("torch's common_quantized.py has no to_blocked/from_blocked")
+    ns = {"torch": torch, "Tensor": torch.Tensor}
+    exec(compile(ast.Module(body=funcs, type_ignores=[]), path, "exec"), ns)
+    return ns["to_blocked"], ns["from_blocked"]
+
+
+@pytest.mark.parametrize("rows,g", [(128, 4), (128, 224), (200, 8), (200, 224), (4096, 4), (4096, 224),
+                                    (4096, 1344), (257, 1344)])
+def test_mx_tiled_scale_layout_equals_torch_to_blocked(rows, g):
+    to_blocked, _ = _torch_block_layout()
+    rng = np.random.default_rng(rows * 7919 + g)
+    s = rng.integers(0, 256, size=(rows, g), dtype=np.uint8)
+    want = to_blocked(torch.from_numpy(s)).numpy()
+    got = oracle.mx_scales_to_tiled(s, fill=0)  # to_blocked pads with zeros
+    assert got.shape == want.shape
+    assert np.array_equal(got, want)
+
+
+def test_mx_tiled_scale_layout_inverts_torch_from_blocked():
+    _, from_blocked = _torch_block_layout()
+    rng = np.random.default_rng(31)
+    for rows, g in [(200, 8), (256, 12)]:
+        s = rng.integers(0, 256, size=(rows, g), dtype=np.uint8)
+        tiled = torch.from_numpy(oracle.mx_scales_to_tiled(s))
+        shape_only = torch.empty((rows, 32 * g), dtype=torch.uint8)
+        back = from_blocked(shape_only, tiled, 32).numpy()
+        assert np.array_equal(back, s)
+
+
+def test_mx_tiled_scale_positions_of_staged_slices():
+    # The staged workload: six 4096 x 7168 slices at scale-column offsets 224 i of one
+    # 4096 x 1344 scale matrix. Every (row, column) of every slice must land where
+    # to_blocked puts it; the element's index is carried through the oracle's layout
+    # in three byte planes and compared with to_blocked of the index matrix.
+    to_blocked, _ = _torch_block_layout()
+    rows, g_total, g_slice = 4096, 1344, 224
+    idx = np.arange(rows * g_total, dtype=np.int64).reshape(rows, g_total)
+    want = to_blocked(torch.from_numpy(idx.astype(np.int32))).numpy().astype(np.int64)
+    got = np.zeros(want.shape, np.int64)
+    for b in range(3):
+        plane = ((idx >> (8 * b)) & 0xFF).astype(np.uint8)
+        got |= oracle.mx_scales_to_tiled(plane).astype(np.int64) << (8 * b)
+    assert np.array_equal(got, want)
+    # and the oracle's per-element offset agrees for sampled elements of each slice
+    rng = np.random.default_rng(32)
+    where = np.empty(want.size, np.int64)
+    where[want] = np.arange(want.size)
+    for i in range(6):
+        for r, c in zip(rng.integers(0, rows, 64), rng.integers(g_slice * i, g_slice * (i + 1), 64)):
+            assert oracle.mx_tiled_scale_offset(int(r), int(c), g_total) == where[r * g_total + c]
 
 
 # ------------------------------------------------------------------ staged == concatenated
