@@ -49,8 +49,24 @@ def _inputs():
     return files
 
 
-def up_to_date(lib: str = LIB) -> bool:
+def _stamp_path(lib: str) -> str:
+    return lib + ".flags"
+
+
+def _flag_stamp(extra_flags) -> str:
+    return "\n".join([*ARCH, *NVCC_FLAGS, *extra_flags]) + "\n"
+
+
+def up_to_date(lib: str = LIB, extra_flags=()) -> bool:
+    """True if `lib` is newer than every source and was built with exactly these flags
+    (recorded in the stamp file written next to it by the build)."""
     if not os.path.exists(lib):
+        return False
+    try:
+        with open(_stamp_path(lib)) as f:
+            if f.read() != _flag_stamp(extra_flags):
+                return False
+    except OSError:
         return False
     t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
@@ -63,13 +79,13 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=(), li
     Concurrent callers (one process per GPU under torchrun) are serialized by a file
     lock: the first builds, the others find the library up to date. The library is
     replaced atomically, so a process that already loaded it is unaffected."""
-    if not force and up_to_date(lib):
+    if not force and up_to_date(lib, extra_flags):
         return lib
     os.makedirs(objdir, exist_ok=True)
     with open(os.path.join(objdir, ".lock"), "w") as lock:
         fcntl.flock(lock, fcntl.LOCK_EX)
         try:
-            if not force and up_to_date(lib):
+            if not force and up_to_date(lib, extra_flags):
                 return lib
             return _build_locked(verbose, extra_flags, lib, objdir)
         finally:
@@ -103,9 +119,14 @@ def _build_locked(verbose: bool, extra_flags, lib: str, objdir: str) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, lib)
+    with open(_stamp_path(lib) + ".tmp", "w") as f:
+        f.write(_flag_stamp(extra_flags))
+    os.replace(_stamp_path(lib) + ".tmp", _stamp_path(lib))
     return lib
 
 
 if __name__ == "__main__":
+    # Extra flags build the default library with them; its stamp then records them, so
+    # the next default build (tests, bench) sees the mismatch and rebuilds.
     flags = sys.argv[1:]
     print(build_library(force=True, verbose=True, extra_flags=flags))
