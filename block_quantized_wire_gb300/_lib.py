@@ -16,7 +16,7 @@ from . import build as _build
 _lock = threading.Lock()
 _lib = None
 
-ABI_VERSION = 4
+ABI_VERSION = 5
 BQ_OK = 0
 STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_ALIAS",
                 5: "BQ_ERR_CUDA"}
@@ -43,6 +43,7 @@ _PROTOS = {
     "bq_dequant_e4m3": ([_P, _P, _I64, _P, _P], ctypes.c_int),
     "bq_reduce_quant_e4m3": ([_P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_take_wait_timeouts": ([_P], ctypes.c_int),
+    "bq_take_wait_unlanded": ([_P], ctypes.c_int),
     "bq_selftest_wait_timeout": ([_P], ctypes.c_int),
 }
 

@@ -385,15 +385,41 @@ bq_status bq_reduce_quant_e4m3(const void *const *x_srcs, int W, int64_t n, uint
                                                    static_cast<uint16_t *>(out_bf16), stream));
 }
 
-bq_status bq_take_wait_timeouts(int64_t *count)
+}  // extern "C"
+
+namespace {
+// Growth of the current device's bounded-wait counter `which` (0: abandoned waits,
+// 1: copies that did not land after one) since the previous call for it. The device
+// counters only grow; the last totals seen are kept per device here, and they are
+// advanced only after every translation unit's counters were read.
+constexpr int kMaxDevices = 64;
+std::mutex g_seen_mu;
+unsigned long long g_seen[kMaxDevices][2];
+
+bq_status take_wait_counter(int which, int64_t *count)
 {
     if (!count) return BQ_ERR_NULL;
-    unsigned long long a = 0, b = 0;
-    if (bqk::take_wait_timeouts_i8(&a) != cudaSuccess || bqk::take_wait_timeouts_mx(&b) != cudaSuccess)
-        return BQ_ERR_CUDA;
-    *count = static_cast<int64_t>(a + b);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BQ_ERR_CUDA;
+    unsigned long long total = 0;
+    for (auto read : {bqk::read_wait_counters_i8, bqk::read_wait_counters_mx_wire, bqk::read_wait_counters_mx,
+                      bqk::read_wait_counters_e4m3}) {
+        unsigned long long v[2] = {0, 0};
+        if (read(v) != cudaSuccess) return BQ_ERR_CUDA;
+        total += v[which];
+    }
+    std::lock_guard<std::mutex> lock(g_seen_mu);
+    *count = static_cast<int64_t>(total - g_seen[dev][which]);
+    g_seen[dev][which] = total;
     return BQ_OK;
 }
+}  // namespace
+
+extern "C" {
+
+bq_status bq_take_wait_timeouts(int64_t *count) { return take_wait_counter(0, count); }
+
+bq_status bq_take_wait_unlanded(int64_t *count) { return take_wait_counter(1, count); }
 
 bq_status bq_selftest_wait_timeout(cudaStream_t stream) { return from_cuda(bqk::launch_wait_selftest(stream)); }
 

@@ -126,13 +126,19 @@ __device__ __forceinline__ void run_staged(const Op &op, int64_t nblk, int chunk
         const uint32_t parity = static_cast<uint32_t>((k / STAGES) & 1);
         // lanes poll on their own clocks; the warp gives up only together
         if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * st, parity, kWaitLimitNs))) {
-            // a copy did not complete in time: record it, let the copies still in
-            // flight (this one included) land, each wait bounded, so no write reaches
-            // freed shared memory, and stop
+            // a copy did not complete in time: record it, give the copies still in
+            // flight (this one included) time to land, each wait bounded, and stop. No
+            // write reaches shared memory after the block exits only if every one of
+            // them lands within its limit; one that does not is counted separately.
             if (lane == 0) atomicAdd(&g_wait_timeouts, 1ull);
-            for (int64_t j = k; j < K && j < k + STAGES; j++)
-                mbar_wait(bar0 + 8 * static_cast<int>(j % STAGES), static_cast<uint32_t>((j / STAGES) & 1),
-                          kWaitLimitNs);
+            for (int64_t j = k; j < K && j < k + STAGES; j++) {
+                const bool landed = mbar_wait(bar0 + 8 * static_cast<int>(j % STAGES),
+                                              static_cast<uint32_t>((j / STAGES) & 1), kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, landed)) {
+                    if (lane == 0) atomicAdd(&g_wait_unlanded, 1ull);
+                    break;
+                }
+            }
             return;
         }
         typename Op::In in;

@@ -34,10 +34,22 @@ __device__ __forceinline__ void pdl_begin()
 // ---------------------------------------------------------------- bulk-copy staging
 // Global -> shared bulk copies (cp.async.bulk, completed on an mbarrier by byte
 // count). Every wait on a barrier is bounded in time: a wait that runs out is counted
-// in g_wait_timeouts (read and cleared by the host through bq_take_wait_timeouts) and
-// the kernel stops early instead of spinning forever.
+// in g_wait_timeouts and the kernel stops early instead of spinning forever. A warp
+// that gave up then waits, again bounded, for its copies still in flight; if one of
+// those waits runs out too, g_wait_unlanded counts it (that block's shared memory may
+// still be written by a copy after the block has exited). Both counters only grow; the
+// host reports their growth since its previous read (bq_take_wait_timeouts,
+// bq_take_wait_unlanded), so no count is lost between a read and a reset.
 static __device__ unsigned long long g_wait_timeouts;
+static __device__ unsigned long long g_wait_unlanded;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Host side: this translation unit's two counters, {timeouts, unlanded}.
+static inline cudaError_t read_wait_counters(unsigned long long (&v)[2])
+{
+    if (cudaError_t e = cudaMemcpyFromSymbol(&v[0], g_wait_timeouts, sizeof v[0])) return e;
+    return cudaMemcpyFromSymbol(&v[1], g_wait_unlanded, sizeof v[1]);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

@@ -147,4 +147,6 @@ cudaError_t launch_reduce_quant_e4m3(const Bf16List &src, int W, int64_t nblk, u
     }
 }
 
+cudaError_t read_wait_counters_e4m3(unsigned long long (&v)[2]) { return read_wait_counters(v); }
+
 }  // namespace bqk

@@ -585,12 +585,7 @@ cudaError_t launch_wait_selftest(cudaStream_t st)
     return cudaGetLastError();
 }
 
-cudaError_t take_wait_timeouts_i8(unsigned long long *count)
-{
-    unsigned long long zero = 0;
-    if (cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof zero)) return e;
-    return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof zero);
-}
+cudaError_t read_wait_counters_i8(unsigned long long (&v)[2]) { return read_wait_counters(v); }
 
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
 {

@@ -93,10 +93,12 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, A
 // the device queries, if any.
 cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem = 0);
 
-// Bounded waits that ran out since the last call, per translation unit (see
-// g_wait_timeouts in bq_device.cuh); each call reads and clears its unit's count.
-cudaError_t take_wait_timeouts_i8(unsigned long long *count);
-cudaError_t take_wait_timeouts_mx(unsigned long long *count);
+// Each kernel translation unit's bounded-wait counters {timeouts, unlanded} (see
+// g_wait_timeouts in bq_device.cuh): totals since the library was loaded, never reset.
+cudaError_t read_wait_counters_i8(unsigned long long (&v)[2]);
+cudaError_t read_wait_counters_mx_wire(unsigned long long (&v)[2]);
+cudaError_t read_wait_counters_mx(unsigned long long (&v)[2]);
+cudaError_t read_wait_counters_e4m3(unsigned long long (&v)[2]);
 cudaError_t launch_wait_selftest(cudaStream_t st);
 
 }  // namespace bqk

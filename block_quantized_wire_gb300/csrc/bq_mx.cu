@@ -337,4 +337,6 @@ cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, 
     return launch_kernel(dequant_mx_kernel<kSegsDequantMx>, grid, st, q, ld_q, s, ld_s, bpr, nblk, out, ld_out);
 }
 
+cudaError_t read_wait_counters_mx(unsigned long long (&v)[2]) { return read_wait_counters(v); }
+
 }  // namespace bqk

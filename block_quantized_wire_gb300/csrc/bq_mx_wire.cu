@@ -465,11 +465,6 @@ cudaError_t launch_ring_hop_mx(const uint8_t *q_in, const uint32_t *s_in, const 
     return launch_hop_mx_stages<kStagesHopMx, false>(q_in, s_in, x, nblk, q, s, nullptr, st);
 }
 
-cudaError_t take_wait_timeouts_mx(unsigned long long *count)
-{
-    unsigned long long zero = 0;
-    if (cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof zero)) return e;
-    return cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof zero);
-}
+cudaError_t read_wait_counters_mx_wire(unsigned long long (&v)[2]) { return read_wait_counters(v); }
 
 }  // namespace bqk

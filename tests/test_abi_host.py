@@ -29,14 +29,14 @@ def test_header_declares_the_calls():
                  "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_quant_mx_f16", "bq_reduce_quant_i8",
                  "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_quant_mx_tiled",
                  "bq_mx_tiled_scale_bytes", "bq_wire_bytes", "bq_status_string",
-                 "bq_abi_version", "bq_take_wait_timeouts", "bq_selftest_wait_timeout"):
+                 "bq_abi_version", "bq_take_wait_timeouts", "bq_take_wait_unlanded", "bq_selftest_wait_timeout"):
         assert want in names
 
 
 def test_library_exports_every_declared_symbol(bq_lib):
     for name in declared_functions():
         assert hasattr(bq_lib, name), name
-    assert bq_lib.bq_abi_version() == 4
+    assert bq_lib.bq_abi_version() == 5
 
 
 def test_wire_bytes_and_status_strings(bq_lib):

@@ -103,7 +103,8 @@ def test_error_vs_unquantized_sum_is_within_half_step_bounds():
 def test_bounded_waits_do_not_run_out_and_can_be_observed():
     # kernels that stage their inputs through bulk copies (the ring hops of the
     # alternative build, which also runs this test) leave no abandoned wait
-    codec.take_wait_timeouts()  # clear whatever earlier tests left
+    codec.take_wait_timeouts()  # consume whatever earlier tests left
+    codec.take_wait_unlanded()
     xs = [x.cuda() for x in inputs.a2a_3072(rows=3072)]
     topology.i8_a2a(xs)
     topology.i8_ring(xs)
@@ -116,6 +117,7 @@ def test_bounded_waits_do_not_run_out_and_can_be_observed():
     torch.cuda.synchronize()
     assert codec.take_wait_timeouts() == 1
     assert codec.take_wait_timeouts() == 0
+    assert codec.take_wait_unlanded() == 0  # the self-test's wait had no copy in flight
     q, s, out = topology.i8_roundtrip(xs[0])
     assert torch.isfinite(out.float()).all()
 
