@@ -368,16 +368,22 @@ __device__ __forceinline__ float2 i8_quotient2(float2 x, float2 r, float2 rl, fl
 // low byte is k in two's complement and k = word - M exactly. |fl(x/s)| <=
 // fl(amax/s) < 127.5, so no clamp is needed there; the flagged path clamps to
 // [-127, 127].
+// The reciprocal path alone, for a block whose scale is known to be >= 2^-100 or 0.
+__device__ __forceinline__ void i8_quant8_fast(const float2 (&v)[4], const I8Scale &b, uint32_t (&w)[8])
+{
+    const float2 r = splat(b.r), rl = splat(b.rl), ns = splat(-b.s), m = splat(kMagic);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float2 y = add2(i8_quotient2(v[i], r, rl, ns), m);
+        w[2 * i] = __float_as_uint(y.x);
+        w[2 * i + 1] = __float_as_uint(y.y);
+    }
+}
+
 __device__ __forceinline__ void i8_quant8(const float2 (&v)[4], const I8Scale &b, uint32_t (&w)[8])
 {
     if (__builtin_expect(b.r >= 0.0f, 1)) {
-        const float2 r = splat(b.r), rl = splat(b.rl), ns = splat(-b.s), m = splat(kMagic);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const float2 y = add2(i8_quotient2(v[i], r, rl, ns), m);
-            w[2 * i] = __float_as_uint(y.x);
-            w[2 * i + 1] = __float_as_uint(y.y);
-        }
+        i8_quant8_fast(v, b, w);
     } else {
 #pragma unroll
         for (int i = 0; i < 8; i++) {
