@@ -38,6 +38,7 @@ _PROTOS = {
     "bq_quant_mx_f16": ([_P, _I64, _I64, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
     "bq_quant_mx_tiled": ([_P, ctypes.c_int, _I64, _I64, _I64, _P, _I64, _P, _I64, _I64, _P], ctypes.c_int),
     "bq_mx_tiled_scale_bytes": ([_I64, _I64], _I64),
+    "bq_quant_mx_slices": ([_P, ctypes.c_int, ctypes.c_int, _I64, _P, _I64, _P, _I64, _P], ctypes.c_int),
     "bq_reduce_quant_i8": ([_P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_quant_e4m3": ([_P, _I64, _P, _P, _P], ctypes.c_int),
     "bq_dequant_e4m3": ([_P, _P, _I64, _P, _P], ctypes.c_int),

@@ -191,6 +191,37 @@ def mx_tiled_scale_bytes(rows: int, g_total: int) -> int:
     return r
 
 
+class _MxSlice(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("cols", ctypes.c_int64), ("ld_x", ctypes.c_int64)]
+
+
+def quant_mx_slices(xs: Sequence[torch.Tensor], q: torch.Tensor, s: torch.Tensor, stream=None) -> None:
+    """Quantize several staged slices (all BF16 or all FP16, each [rows, cols_i]) in one
+    launch into q [rows, sum cols_i] and s [rows, sum cols_i / 32], slice i at the columns
+    after slice i-1's: the bytes of quant_mx called once per slice (bq_quant_mx_slices)."""
+    if not 1 <= len(xs) <= 16:
+        raise ValueError("quant_mx_slices: 1 to 16 slices")
+    f16 = xs[0].dtype == torch.float16
+    dt = torch.float16 if f16 else torch.bfloat16
+    arr = (_MxSlice * len(xs))()
+    rows = None
+    total = 0
+    for i, x in enumerate(xs):
+        xp, r, c, ld = _rows(x, dt, f"xs[{i}]")
+        if rows is None:
+            rows = r
+        elif r != rows:
+            raise ValueError("quant_mx_slices: every slice must have the same number of rows")
+        arr[i] = _MxSlice(xp, c, ld)
+        total += c
+    qp, qr, qc, ld_q = _rows(q, torch.uint8, "q")
+    sp, sr, sc, ld_s = _rows(s, torch.uint8, "s")
+    if (qr, qc) != (rows, total) or (sr, sc) != (rows, total // GROUP_MX):
+        raise ValueError("quant_mx_slices: q and s must cover the slices' rows and total columns")
+    check("bq_quant_mx_slices", load().bq_quant_mx_slices(arr, len(xs), int(f16), rows, qp, ld_q, sp, ld_s,
+                                                          _stream(stream)))
+
+
 def quant_mx_tiled(x: torch.Tensor, q: torch.Tensor, s_tiled: torch.Tensor, g_total: int, g0: int = 0,
                    stream=None) -> None:
     """BF16 or FP16 x [rows, cols] -> E4M3 q [rows, cols] and E8M0 scales written into the

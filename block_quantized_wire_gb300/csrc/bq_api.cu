@@ -307,6 +307,42 @@ bq_status bq_quant_mx_tiled(const void *x, int x_is_f16, int64_t rows, int64_t c
                                                 q_e4m3, ld_q, s_tiled, g_total / 4, g0 / 4, stream));
 }
 
+bq_status bq_quant_mx_slices(const bq_mx_slice *slices, int nslices, int x_is_f16, int64_t rows, uint8_t *q_e4m3,
+                             int64_t ld_q, uint8_t *s_e8m0, int64_t ld_s, cudaStream_t stream)
+{
+    if (nslices < 1 || nslices > BQ_MAX_SLICES || rows < 0) return BQ_ERR_SHAPE;
+    if (!slices) return BQ_ERR_NULL;
+    int64_t total = 0;
+    for (int i = 0; i < nslices; i++) {
+        const int64_t c = slices[i].cols;
+        if (c < 0 || c % 128 || slices[i].ld_x < c) return BQ_ERR_SHAPE;
+        total += c;
+    }
+    if (rows == 0 || total == 0) return BQ_OK;
+    if (ld_q < total || ld_s < total / BQ_GROUP_MX) return BQ_ERR_SHAPE;
+    if (!q_e4m3 || !s_e8m0) return BQ_ERR_NULL;
+    if (!aligned(q_e4m3, 16) || ld_q % 16 || !aligned(s_e8m0, 4) || ld_s % 4) return BQ_ERR_ALIGN;
+    Range ins[BQ_MAX_SLICES];
+    bqk::MxSliceList sl = {};
+    int64_t col = 0;
+    for (int i = 0; i < nslices; i++) {
+        const int64_t c = slices[i].cols;
+        if (c == 0) continue;
+        if (!slices[i].x) return BQ_ERR_NULL;
+        if (!aligned(slices[i].x, 16) || slices[i].ld_x % 8) return BQ_ERR_ALIGN;
+        ins[sl.n] = span2d(slices[i].x, rows, 2 * c, 2 * slices[i].ld_x);
+        sl.x[sl.n] = static_cast<const uint16_t *>(slices[i].x);
+        sl.ld_x[sl.n] = slices[i].ld_x;
+        sl.bpr[sl.n] = c / 128;
+        sl.cb0[sl.n] = col / 128;
+        sl.n++;
+        col += c;
+    }
+    const Range outs[] = {span2d(q_e4m3, rows, total, ld_q), span2d(s_e8m0, rows, total / BQ_GROUP_MX, ld_s)};
+    if (any_alias(outs, 2, ins, sl.n)) return BQ_ERR_ALIAS;
+    return from_cuda(bqk::launch_quant_mx_slices(sl, x_is_f16 != 0, rows, q_e4m3, ld_q, s_e8m0, ld_s, stream));
+}
+
 int64_t bq_mx_tiled_scale_bytes(int64_t rows, int64_t g_total)
 {
     if (rows < 0 || g_total < 0 || g_total % 4) return -1;

@@ -21,6 +21,19 @@ struct WireList {
 using SourceList = WireList<int8_t, float>;       // block INT8: one FP32 scale per block
 using MxSourceList = WireList<uint8_t, uint32_t>;  // MXFP8: four E8M0 bytes per block
 
+// Staged MX slices quantized by one launch: slice i is x[i] [rows, 128 * bpr[i]] with
+// leading dimension ld_x[i], written at 128-column block cb0[i] of the destination;
+// cta0 is filled by the launcher.
+constexpr int kMaxSlices = 16;
+struct MxSliceList {
+    const uint16_t *x[kMaxSlices];
+    int64_t ld_x[kMaxSlices];
+    int64_t bpr[kMaxSlices];
+    int64_t cb0[kMaxSlices];
+    int cta0[kMaxSlices + 1];
+    int n;
+};
+
 // BF16 shards of the W ranks, in rank order (the reduce of the all-gather modes).
 struct Bf16List {
     const uint16_t *x[kMaxSources];
@@ -46,6 +59,8 @@ cudaError_t launch_quant_mx_f16(const uint16_t *x, int64_t ld_x, int64_t rows, i
                                 int64_t ld_q, uint8_t *s, int64_t ld_s, cudaStream_t st);
 cudaError_t launch_quant_mx_tiled(const uint16_t *x, bool f16, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,
                                   int64_t ld_q, uint8_t *s_tiled, int64_t tiles_per_row, int64_t c0, cudaStream_t st);
+cudaError_t launch_quant_mx_slices(MxSliceList sl, bool f16, int64_t rows, uint8_t *q, int64_t ld_q, uint8_t *s,
+                                   int64_t ld_s, cudaStream_t st);
 cudaError_t launch_reduce_quant_i8(const Bf16List &src, int W, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                                    cudaStream_t st);
 cudaError_t launch_quant_e4m3(const uint16_t *x, int64_t nblk, uint8_t *q, float *s, cudaStream_t st);

@@ -167,11 +167,12 @@ struct ChunkWalkT {
     int64_t c, stride, b0, step;
     ChunkPos pos;
     int64_t drow, dcb, bpr;
-    __device__ __forceinline__ ChunkWalkT(int64_t bpr_)
+    // cta, ncta: this CTA's index among the ncta CTAs that share the walk
+    __device__ __forceinline__ ChunkWalkT(int64_t bpr_, int64_t cta, int64_t ncta)
     {
         bpr = bpr_;
-        stride = ((int64_t)gridDim.x * kThreads) >> 5;
-        c = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+        stride = (ncta * kThreads) >> 5;
+        c = (cta * kThreads + threadIdx.x) >> 5;
         b0 = c * CB;
         pos.row0 = b0 / bpr;
         pos.cb0 = b0 - pos.row0 * bpr;
@@ -200,17 +201,17 @@ using ChunkWalk = ChunkWalkT<kChunkBlocks>;
 #define BQ_QUANT_MX_MIN_CTAS 4
 #endif
 
+// Quantize one [rows, bpr * 128] matrix with ncta CTAs, this one being number cta.
 // kF16: the input is FP16 instead of BF16. kTiled: scales go to the tiled GEMM layout
 // (see scale_offset), c0 the slice's first tile column.
 template <bool kF16, bool kTiled>
-__global__ void __launch_bounds__(kThreads, BQ_QUANT_MX_MIN_CTAS)
-quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
-                int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s, int64_t c0)
+__device__ __forceinline__ void quant_mx_matrix(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk,
+                                                uint8_t *__restrict__ q, int64_t ld_q, uint8_t *__restrict__ s,
+                                                int64_t ld_s, int64_t c0, int64_t cta, int64_t ncta)
 {
-    pdl_begin();
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
-    ChunkWalk w(bpr);
+    ChunkWalk w(bpr, cta, ncta);
     for (; w.c < nfull; w.next()) {
         uint4 raw[kSegs];
         quant_mx_load_any<false>(x, ld_x, bpr, nblk, w.b0, w.pos, lane, raw);
@@ -221,6 +222,32 @@ quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64
         quant_mx_load_any<true>(x, ld_x, bpr, nblk, w.b0, w.pos, lane, raw);
         quant_mx_compute_any<kF16, kTiled, true>(raw, bpr, nblk, q, ld_q, s, ld_s, c0, w.b0, w.pos, lane);
     }
+}
+
+template <bool kF16, bool kTiled>
+__global__ void __launch_bounds__(kThreads, BQ_QUANT_MX_MIN_CTAS)
+quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
+                int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s, int64_t c0)
+{
+    pdl_begin();
+    quant_mx_matrix<kF16, kTiled>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, blockIdx.x, gridDim.x);
+}
+
+// Several staged slices in one launch (bq_quant_mx_slices): the CTAs are split between
+// the slices in proportion to their work, CTAs [cta0[i], cta0[i + 1]) taking slice i;
+// each CTA finds its slice once and then walks that slice's chunks exactly as a launch
+// of the slice alone would, with its slice-local index and the slice's CTA count.
+template <bool kF16>
+__global__ void __launch_bounds__(kThreads, BQ_QUANT_MX_MIN_CTAS)
+quant_mx_slices_kernel(const __grid_constant__ MxSliceList sl, int64_t rows, uint8_t *__restrict__ q, int64_t ld_q,
+                       uint8_t *__restrict__ s, int64_t ld_s)
+{
+    pdl_begin();
+    int i = 0;
+    while (i + 1 < sl.n && static_cast<int>(blockIdx.x) >= sl.cta0[i + 1]) ++i;
+    const int64_t bpr = sl.bpr[i];
+    quant_mx_matrix<kF16, false>(sl.x[i], sl.ld_x[i], bpr, rows * bpr, q + 128 * sl.cb0[i], ld_q, s + 4 * sl.cb0[i],
+                                 ld_s, 0, static_cast<int64_t>(blockIdx.x) - sl.cta0[i], sl.cta0[i + 1] - sl.cta0[i]);
 }
 
 // Materialize one chunk of SEGS segments (2 * SEGS blocks); all loads of the chunk are
@@ -276,7 +303,7 @@ dequant_mx_kernel(const uint8_t *__restrict__ q, int64_t ld_q, const uint8_t *__
     const int lane = threadIdx.x & 31;
     constexpr int CB = 2 * SEGS;
     const int64_t nfull = nblk / CB;
-    ChunkWalkT<CB> w(bpr);
+    ChunkWalkT<CB> w(bpr, blockIdx.x, gridDim.x);
     for (; w.c < nfull; w.next())
         dequant_mx_chunk_any<SEGS, false>(q, ld_q, s, ld_s, bpr, nblk, out, ld_out, w.b0, w.pos, lane);
     if (w.c == nfull && nblk % CB)
@@ -319,6 +346,43 @@ cudaError_t launch_quant_mx_f16(const uint16_t *x, int64_t ld_x, int64_t rows, i
                                 uint8_t *s, int64_t ld_s, cudaStream_t st)
 {
     return launch_quant_mx_any<true, false>(x, ld_x, rows, cols, q, ld_q, s, ld_s, 0, st);
+}
+
+// Work split of a slice batch: grid CTAs (at least one per slice) in proportion to
+// each slice's chunks, no slice given more CTAs than its warps have chunks for.
+cudaError_t launch_quant_mx_slices(MxSliceList sl, bool f16, int64_t rows, uint8_t *q, int64_t ld_q, uint8_t *s,
+                                   int64_t ld_s, cudaStream_t st)
+{
+    auto kernel = f16 ? quant_mx_slices_kernel<true> : quant_mx_slices_kernel<false>;
+    int64_t chunks[kMaxSlices], total = 0;
+    for (int i = 0; i < sl.n; i++) {
+        chunks[i] = (rows * sl.bpr[i] + kChunkBlocks - 1) / kChunkBlocks;
+        total += chunks[i];
+    }
+    BQK_GRID(kernel, total);
+    constexpr int64_t kWarps = kThreads / 32;
+    int64_t ctas[kMaxSlices], used = 0;
+    for (int i = 0; i < sl.n; i++) {
+        const int64_t most = (chunks[i] + kWarps - 1) / kWarps;
+        int64_t c = static_cast<int64_t>(grid) * chunks[i] / total;
+        c = c < 1 ? 1 : (c > most ? most : c);
+        ctas[i] = c;
+        used += c;
+    }
+    // CTAs left over by the rounding go, one at a time, to the slice with the most
+    // chunks per CTA that can still take one
+    for (; used < grid; used++) {
+        int best = -1;
+        for (int i = 0; i < sl.n; i++)
+            if (ctas[i] < (chunks[i] + kWarps - 1) / kWarps &&
+                (best < 0 || chunks[i] * ctas[best] > chunks[best] * ctas[i]))
+                best = i;
+        if (best < 0) break;
+        ctas[best]++;
+    }
+    sl.cta0[0] = 0;
+    for (int i = 0; i < sl.n; i++) sl.cta0[i + 1] = sl.cta0[i] + static_cast<int>(ctas[i]);
+    return launch_kernel(kernel, sl.cta0[sl.n], st, sl, rows, q, ld_q, s, ld_s);
 }
 
 cudaError_t launch_quant_mx_tiled(const uint16_t *x, bool f16, int64_t ld_x, int64_t rows, int64_t cols, uint8_t *q,

@@ -234,6 +234,32 @@ BQ_API bq_status bq_quant_mx_tiled(const void *x, int x_is_f16, int64_t rows, in
                             uint8_t *q_e4m3, int64_t ld_q, uint8_t *s_tiled, int64_t g_total,
                             int64_t g0, cudaStream_t stream);
 
+/* Several staged slices quantized by one call: the bytes of bq_quant_mx (BF16, or
+ * bq_quant_mx_f16 when x_is_f16 != 0) called once per slice, slice i at the
+ * destination columns that follow slice i - 1's ("[II] Support staged MXFP8 linear
+ * inputs", Behavior: quantize_input_slice writes a 128-column-aligned slice at its
+ * offset of the assembled input). One launch covers every slice, so slices that are
+ * ready together do not pay one launch's ramp and tail each.
+ *   slices[i].x      [rows][slices[i].ld_x] BF16 or FP16 (read); 16-byte aligned,
+ *                    ld_x % 8 == 0, ld_x >= cols
+ *   slices[i].cols   a multiple of 128 (0: the slice is skipped); slice i starts at
+ *                    column c_i = cols_0 + ... + cols_(i-1) of the destination
+ *   nslices          1 <= nslices <= BQ_MAX_SLICES; the slices array is host memory
+ *   q_e4m3, s_e8m0   the destination's first column: [rows][ld_q] and [rows][ld_s]
+ *                    (written), as in bq_quant_mx, for the total of the slices'
+ *                    columns; offset them for a batch that starts at another
+ *                    128-column-aligned column
+ * Slices may overlap one another; the outputs may overlap none of them. */
+typedef struct bq_mx_slice {
+    const void *x;
+    int64_t cols;
+    int64_t ld_x;
+} bq_mx_slice;
+#define BQ_MAX_SLICES 16
+BQ_API bq_status bq_quant_mx_slices(const bq_mx_slice *slices, int nslices, int x_is_f16, int64_t rows,
+                                    uint8_t *q_e4m3, int64_t ld_q, uint8_t *s_e8m0, int64_t ld_s,
+                                    cudaStream_t stream);
+
 /* Bytes of the tiled scale layout for rows x g_total scales (rows rounded up to 128);
  * -1 if g_total is not a non-negative multiple of 4. */
 BQ_API int64_t bq_mx_tiled_scale_bytes(int64_t rows, int64_t g_total);

@@ -27,7 +27,7 @@ def test_header_declares_the_calls():
     names = declared_functions()
     for want in ("bq_quant_i8", "bq_dequant_i8", "bq_dequant_accum_i8", "bq_ring_hop_i8", "bq_quant_mx",
                  "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_quant_mx_f16", "bq_reduce_quant_i8",
-                 "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_quant_mx_tiled",
+                 "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_quant_mx_tiled", "bq_quant_mx_slices",
                  "bq_mx_tiled_scale_bytes", "bq_wire_bytes", "bq_status_string",
                  "bq_abi_version", "bq_take_wait_timeouts", "bq_take_wait_unlanded", "bq_selftest_wait_timeout"):
         assert want in names
@@ -220,6 +220,40 @@ def test_quant_mx_tiled_rejections(bq_lib):
     assert bq_lib.bq_mx_tiled_scale_bytes(256, 8) == 2 * 2 * 512
     assert bq_lib.bq_mx_tiled_scale_bytes(300, 1344) == 3 * 336 * 512
     assert bq_lib.bq_mx_tiled_scale_bytes(1, 6) == -1
+
+
+def test_quant_mx_slices_rejections(bq_lib):
+    from block_quantized_wire_gb300.codec import _MxSlice
+    f = bq_lib.bq_quant_mx_slices
+    q, s = A + 0x10000000, A + 0x20000000
+
+    def sl(*specs):
+        arr = (_MxSlice * len(specs))()
+        for i, (x, cols, ld) in enumerate(specs):
+            arr[i] = _MxSlice(x, cols, ld)
+        return arr
+
+    two = sl((A, 256, 256), (A + 0x1000000, 128, 128))
+    assert f(two, 0, 0, 64, q, 384, s, 12, None) == SHAPE                   # no slices
+    assert f(sl(*[(A, 128, 128)] * 17), 17, 0, 64, q, 17 * 128, s, 68, None) == SHAPE  # too many
+    assert f(None, 2, 0, 64, q, 384, s, 12, None) == NULL
+    assert f(two, 2, 0, -1, q, 384, s, 12, None) == SHAPE
+    assert f(sl((A, 200, 256)), 1, 0, 64, q, 256, s, 8, None) == SHAPE    # cols % 128
+    assert f(sl((A, 256, 128)), 1, 0, 64, q, 256, s, 8, None) == SHAPE    # ld_x < cols
+    assert f(two, 2, 0, 0, None, 384, None, 12, None) == OK               # no rows: nothing to do
+    assert f(sl((A, 0, 0), (None, 0, 0)), 2, 0, 64, None, 0, None, 0, None) == OK  # no columns
+    assert f(two, 2, 0, 64, q, 256, s, 12, None) == SHAPE                 # ld_q < total columns
+    assert f(two, 2, 0, 64, q, 384, s, 8, None) == SHAPE                  # ld_s < total / 32
+    assert f(two, 2, 0, 64, None, 384, s, 12, None) == NULL
+    assert f(sl((A, 256, 256), (None, 128, 128)), 2, 0, 64, q, 384, s, 12, None) == NULL
+    assert f(sl((A, 256, 256), (None, 0, 0)), 2, 0, 0, q, 384, s, 12, None) == OK  # empty slice skipped
+    assert f(sl((A + 8, 256, 256)), 1, 1, 64, q, 256, s, 8, None) == ALIGN  # x 16-byte aligned
+    assert f(sl((A, 256, 260)), 1, 0, 64, q, 256, s, 8, None) == ALIGN      # ld_x % 8
+    assert f(two, 2, 0, 64, q, 392, s, 12, None) == ALIGN                 # ld_q % 16
+    assert f(two, 2, 0, 64, q, 384, s + 2, 12, None) == ALIGN
+    assert f(two, 2, 0, 64, A + 0x1000000 + 512, 384, s, 12, None) == ALIAS  # q over slice 1
+    assert f(two, 2, 0, 64, q, 384, A + 64, 12, None) == ALIAS              # s over slice 0
+    assert f(two, 2, 0, 64, q, 384, q + 256, 12, None) == ALIAS             # s over q
 
 
 def test_mx_rejections(bq_lib):

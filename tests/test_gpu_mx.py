@@ -165,3 +165,79 @@ def test_mx_empty_is_noop():
     codec.quant_mx(x, q, s)
     codec.dequant_mx(q, s, torch.empty((0, 128), dtype=torch.bfloat16, device="cuda"))
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ several slices in one call
+def _slices_vs_oracle(widths, rows, dtype, seed, ld_pad=0, col_off=0):
+    """Slices of the given widths (views into wider tensors when ld_pad > 0) quantized by
+    one bq_quant_mx_slices call into a destination that starts at column col_off of a
+    guarded wider buffer; compared with the oracle on the concatenation and with one
+    bq_quant_mx call per slice."""
+    rng = np.random.default_rng(seed)
+    xs = []
+    for w in widths:
+        xf = (rng.standard_normal((rows, w + ld_pad)) * 0.02).astype(np.float32)
+        xf[rng.random(xf.shape) < 0.002] *= 100
+        full = torch.from_numpy(xf).to(dtype).cuda()
+        xs.append(full[:, :w])
+    total = sum(widths)
+    C = col_off + total + 128
+    gq = Guarded(rows * C)
+    gs = Guarded(rows * (C // 32))
+    q_all = gq.view(torch.uint8, (rows, C))
+    s_all = gs.view(torch.uint8, (rows, C // 32))
+    q = q_all[:, col_off:col_off + total]
+    s = s_all[:, col_off // 32:(col_off + total) // 32]
+    codec.quant_mx_slices(xs, q, s)
+    torch.cuda.synchronize()
+    assert gq.bands_intact() and gs.bands_intact()
+    untouched_q = torch.cat([q_all[:, :col_off], q_all[:, col_off + total:]], dim=1)
+    assert bool((untouched_q == Guarded.SENTINEL).all())
+    fmt = "f16" if dtype == torch.float16 else "bf16"
+    cat = torch.cat([x.contiguous() for x in xs if x.shape[1]], dim=1)
+    q_ref, s_ref = oracle.quant_mx(cat.view(torch.int16).cpu().numpy().view(np.uint16), fmt=fmt)
+    assert_same(q.contiguous(), q_ref, "E4M3 codes")
+    assert_same(s.contiguous(), s_ref, "E8M0 scales")
+    # the same bytes as one quant_mx call per slice
+    q1, s1 = codec.empty_mx(rows, total)
+    c = 0
+    for x in xs:
+        w = x.shape[1]
+        if w:
+            codec.quant_mx(x, q1[:, c:c + w], s1[:, c // 32:(c + w) // 32])
+        c += w
+    assert torch.equal(q1, q) and torch.equal(s1, s)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_slices_in_one_call_ragged_widths(dtype):
+    # unequal widths, strided views, a destination offset, rows that end mid-chunk
+    _slices_vs_oracle([128, 384, 256, 1024, 128, 640], rows=300, dtype=dtype, seed=41, ld_pad=64, col_off=256)
+
+
+def test_slices_in_one_call_sixteen_narrow_slices_and_an_empty_one():
+    _slices_vs_oracle([128] * 7 + [0] + [128] * 8, rows=37, dtype=torch.bfloat16, seed=42)
+
+
+def test_slices_in_one_call_single_slice_and_single_row():
+    _slices_vs_oracle([7168], rows=1, dtype=torch.bfloat16, seed=43)
+    _slices_vs_oracle([256, 128], rows=5, dtype=torch.float16, seed=44, ld_pad=8)
+
+
+def test_slices_in_one_call_staged_workload():
+    # the staged workload at full size: six 4096 x 7168 slices into 4096 x 43008 in one
+    # call equal six bq_quant_mx calls byte for byte; sampled rows against the oracle
+    slices = inputs.mx_slices_4096()
+    rows, cols = slices[0].shape
+    C = len(slices) * cols
+    q, s = codec.empty_mx(rows, C)
+    codec.quant_mx_slices(slices, q, s)
+    q1, s1 = codec.empty_mx(rows, C)
+    for i, x in enumerate(slices):
+        codec.quant_mx(x, q1[:, i * cols:(i + 1) * cols], s1[:, i * cols // 32:(i + 1) * cols // 32])
+    assert torch.equal(q, q1) and torch.equal(s, s1)
+    pick = torch.tensor([0, 1, 2047, 4094, 4095], device="cuda")
+    cat = torch.cat([x[pick] for x in slices], dim=1)
+    q_ref, s_ref = oracle.quant_mx(bits(cat))
+    assert_same(q[pick], q_ref, "E4M3 codes")
+    assert_same(s[pick], s_ref, "E8M0 scales")
