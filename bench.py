@@ -46,6 +46,7 @@ HIDDEN = 7168
 W_SRC = 4
 N_SLICES = 6
 BF16 = 2
+RAW_SAMPLES = 200  # raw timing samples kept per series in the JSON line
 
 
 def wire_per_value() -> float:
@@ -69,6 +70,9 @@ def kernel_bytes(name: str, n: int) -> int:
         "quant_e4m3": BF16 + w,
         "dequant_e4m3": w + BF16,
         "quant_mx_f16": BF16 + w,
+        "quant_mx_slices": BF16 + w,
+        "quant_mx_tiled": BF16 + w,
+        "quant_mx_tiled_f16": BF16 + w,
     }[name]
     return int(round(per * n))
 
@@ -149,9 +153,98 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()[:16]
 
 
+class NvmlClocks:
+    """SM clock, its maximum, power and throttle reasons read in-process through NVML
+    (ctypes on libnvidia-ml; read-only queries). A thread samples every `period_s`
+    between mark_start() and mark_stop(), and both marks take a sample themselves, so
+    even a 40 ms timed region has a dozen or more samples of its own."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, device: torch.device, period_s: float = 0.002):
+        import ctypes
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        self._run = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device)
+            uuid = str(getattr(props, "uuid", ""))
+            bus = "%04x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), getattr(props, "pci_bus_id", 0),
+                                        getattr(props, "pci_device_id", 0))
+            found = False
+            if uuid:
+                u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                found = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+            for b in ([] if found else [bus, "0000" + bus]):
+                found = found or nv.nvmlDeviceGetHandleByPciBusId_v2(b.encode(), ctypes.byref(h)) == 0
+            if not found:
+                return
+            self.nv, self.h, self.ct = nv, h, ctypes
+            try:
+                self.reasons_fn = nv.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                self.reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # NVML_CLOCK_SM
+                return
+            self.max_mhz = float(mx.value)
+            self.ok = self._sample() is not None
+        except (OSError, AttributeError, RuntimeError):
+            self.ok = False
+
+    def _sample(self):
+        ct, nv, h = self.ct, self.nv, self.h
+        sm, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(sm)) != 0:
+            return None
+        p = float(pw.value) / 1000.0 if nv.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) == 0 else None
+        r = int(rs.value) if self.reasons_fn(h, ct.byref(rs)) == 0 else 0
+        s = (float(sm.value), p, r)
+        self.samples.append(s)
+        return s
+
+    def _loop(self):
+        while self._run:
+            self._sample()
+            time.sleep(self.period)
+
+    def mark_start(self):
+        if not self.ok:
+            return
+        self.samples = []
+        self._sample()
+        self._run = True
+        self._t = threading.Thread(target=self._loop, daemon=True)
+        self._t.start()
+
+    def mark_stop(self):
+        if not self.ok:
+            return
+        self._run = False
+        self._t.join(timeout=2)
+        self._sample()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        sms = [s[0] for s in self.samples]
+        pw = [s[1] for s in self.samples if s[1] is not None]
+        reasons = sorted({nm for s in self.samples for bit, nm in self.REASONS.items() if s[2] & bit})
+        return {"sm_mhz": statistics.median(sms), "sm_mhz_min": min(sms), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sms), "power_w_max": max(pw) if pw else None,
+                "source": f"NVML in-process every {self.period * 1e3:.0f} ms plus one read at each end of the region"}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 100 ms; only samples taken
-    between mark_start() and mark_stop() (the timed region) are summarized."""
+    between mark_start() and mark_stop() (the timed region) are summarized. The fallback
+    when NVML cannot be read in-process."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -419,11 +512,15 @@ def cpu_inputs(rows: int, slice_rows: int):
 
 
 # ---------------------------------------------------------------- widened rows
-def graph_ms(fn, reps: int) -> float:
-    """Average device time of one call of fn: `reps` calls captured into one CUDA graph
-    (after 3 eager warm-ups) and the graph timed by CUDA events around one replay, so
-    the host's launch overhead is not in the number (short launches would otherwise
-    wait for the host)."""
+GRAPH_REPLAYS = 5
+
+
+def graph_stats(fn, reps: int, replays: int = GRAPH_REPLAYS):
+    """Device time of one call of fn: `reps` calls captured into one CUDA graph (after 3
+    eager warm-ups), the graph replayed `replays` times with CUDA events around each
+    replay, so the host's launch overhead is not in the number (short launches would
+    otherwise wait for the host). Returns the median per-call time (ms) and the
+    per-replay samples."""
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -436,14 +533,27 @@ def graph_ms(fn, reps: int) -> float:
             fn()
     g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    samples = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        samples.append(e0.elapsed_time(e1) / reps)
     del g
-    return ms
+    return statistics.median(samples), samples
+
+
+def graph_ms(fn, reps: int) -> float:
+    return graph_stats(fn, reps)[0]
+
+
+def spread(samples) -> dict:
+    """Median, min, max (us) and the raw per-replay samples of graph_stats."""
+    return {"replays": len(samples), "median_us": round(statistics.median(samples) * 1e3, 2),
+            "min_us": round(min(samples) * 1e3, 2), "max_us": round(max(samples) * 1e3, 2),
+            "samples_us": [round(t * 1e3, 2) for t in samples]}
 
 
 def time_next_rows(pipe, args, peak):
@@ -476,7 +586,20 @@ def time_next_rows(pipe, args, peak):
         c0 = i * HIDDEN
         c.quant_mx(f16[i], pipe.mx_q[:, c0:c0 + HIDDEN], pipe.mx_s[:, c0 // 32:(c0 + HIDDEN) // 32])
 
+    g_total = N_SLICES * HIDDEN // 32
+    tiled = torch.zeros((c.mx_tiled_scale_bytes(pipe.slice_rows, g_total),), dtype=torch.uint8, device=dev)
+
+    def quant_tiled(xs_, turn_):
+        i = turn_[0] % len(xs_)
+        turn_[0] += 1
+        c0 = i * HIDDEN
+        c.quant_mx_tiled(xs_[i], pipe.mx_q[:, c0:c0 + HIDDEN], tiled, g_total, c0 // 32)
+
+    turn_t, turn_t16 = [0], [0]
     runs = {
+        "quant_mx_slices": (lambda: c.quant_mx_slices(pipe.slices, pipe.mx_q, pipe.mx_s), ns * N_SLICES),
+        "quant_mx_tiled": (lambda: quant_tiled(pipe.slices, turn_t), ns),
+        "quant_mx_tiled_f16": (lambda: quant_tiled(f16, turn_t16), ns),
         "dequant_accum_mx": (lambda: c.dequant_accum_mx([wires[w][1] for w in range(W_SRC)],
                                                         [wires[w][2] for w in range(W_SRC)], acc[1], acc[2], None), n),
         "ring_hop_mx": (lambda: c.ring_hop_mx(wires[0][1], wires[0][2], xs[1], hop[1], hop[2], None), n),
@@ -488,12 +611,14 @@ def time_next_rows(pipe, args, peak):
     }
     out = {}
     for name, (fn, nv) in runs.items():
-        avg_ms = graph_ms(fn, args.next_reps)
+        avg_ms, samples = graph_stats(fn, args.next_reps)
         nbytes = kernel_bytes(name, nv)
         gbs = nbytes / (avg_ms * 1e-3) / 1e9
         out[name] = {"launches": args.next_reps, "avg_us": round(avg_ms * 1e3, 2), "bytes_per_launch": nbytes,
-                     "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
-    del wires, ew, iw, f16
+                     "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4), **spread(samples)}
+    out["quant_mx_slices"]["what"] = ("the six staged slices of the step quantized by one bq_quant_mx_slices "
+                                      "call (one launch) instead of six bq_quant_mx calls")
+    del wires, ew, iw, f16, tiled
     return out
 
 
@@ -510,7 +635,7 @@ def time_configs(args, peak):
     out = {}
 
     def timed(fn, name, n, cfg):
-        ms = graph_ms(fn, args.next_reps)
+        ms, samples = graph_stats(fn, args.next_reps)
         nbytes = kernel_bytes(name, n) if name in ("quant_i8", "dequant_i8", "quant_mx", "dequant_mx",
                                                    "dequant_accum_i8", "ring_hop_i8") else None
         if name == "dequant_accum_i8+bf16":
@@ -518,7 +643,7 @@ def time_configs(args, peak):
         gbs = nbytes / (ms * 1e-3) / 1e9
         out.setdefault(cfg, {})[name] = {"avg_us": round(ms * 1e3, 2), "bytes_per_launch": nbytes,
                                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                                         "l2": "warm" if nbytes < L2 else "cold"}
+                                         "l2": "warm" if nbytes < L2 else "cold", **spread(samples)}
 
     x1 = inputs.roundtrip_512(device=dev)
     _, q1, s1 = codec.empty_wire_i8(x1.numel(), dev)
@@ -554,6 +679,81 @@ def time_configs(args, peak):
     return out
 
 
+# ---------------------------------------------------------------- one kernel alone (profiling)
+PROFILE_OPS = ("quant_i8", "dequant_i8", "dequant_accum_i8", "ring_hop_i8", "quant_mx", "dequant_mx",
+               "quant_mx_slices", "dequant_accum_mx", "ring_hop_mx")
+
+
+def run_profile_op(args):
+    """Launch one kernel of the workload `--profile-launches` times after `--warmup`
+    launches, holding only that kernel's buffers (the prefill buffers at --rows, or the
+    staged slices at --slice-rows), so that a profiler can capture one launch of a full-size
+    kernel with a few GB on the device. Prints one line with the launch count; the
+    timings of a run under a profiler are not benchmark values."""
+    from block_quantized_wire_gb300 import build as bq_build, codec, inputs
+    bq_build.build_library()
+    dev = torch.device("cuda", 0)
+    op, rows = args.profile_op, args.rows
+    n = rows * HIDDEN
+    if op in ("quant_mx", "quant_mx_slices", "dequant_mx"):
+        sl = inputs.mx_slices_4096(device=dev, rows=args.slice_rows)
+        q, s = codec.empty_mx(args.slice_rows, HIDDEN * N_SLICES, dev)
+        turn = [0]
+
+        def one_slice():
+            i = turn[0] % N_SLICES
+            turn[0] += 1
+            c0 = i * HIDDEN
+            codec.quant_mx(sl[i], q[:, c0:c0 + HIDDEN], s[:, c0 // 32:(c0 + HIDDEN) // 32])
+        codec.quant_mx_slices(sl, q, s)
+        if op == "dequant_mx":
+            del sl
+            out = torch.empty((args.slice_rows, HIDDEN * N_SLICES), dtype=torch.bfloat16, device=dev)
+            fn = lambda: codec.dequant_mx(q, s, out)
+        else:
+            fn = one_slice if op == "quant_mx" else (lambda: codec.quant_mx_slices(sl, q, s))
+    elif op in ("dequant_accum_mx", "ring_hop_mx"):
+        nsrc = W_SRC if op == "dequant_accum_mx" else 1
+        wires = [codec.empty_wire_mx(n, dev) for _ in range(nsrc)]
+        for w in range(nsrc):
+            x = inputs.prefill_buffer(w, device=dev, rows=rows)
+            codec.quant_mx_flat(x.view(-1), wires[w][1], wires[w][2])
+            del x
+        o = codec.empty_wire_mx(n, dev)
+        if op == "dequant_accum_mx":
+            fn = lambda: codec.dequant_accum_mx([w[1] for w in wires], [w[2] for w in wires], o[1], o[2], None)
+        else:
+            xl = inputs.prefill_buffer(1, device=dev, rows=rows).view(-1)
+            fn = lambda: codec.ring_hop_mx(wires[0][1], wires[0][2], xl, o[1], o[2], None)
+    else:
+        nsrc = {"quant_i8": 0, "dequant_i8": 1, "dequant_accum_i8": W_SRC, "ring_hop_i8": 1}[op]
+        wires = [codec.empty_wire_i8(n, dev) for _ in range(nsrc)]
+        for w in range(nsrc):
+            x = inputs.prefill_buffer(w, device=dev, rows=rows)
+            codec.quant_i8(x.view(-1), wires[w][1], wires[w][2])
+            del x
+        o = codec.empty_wire_i8(n, dev)
+        if op == "quant_i8":
+            x0 = inputs.prefill_buffer(0, device=dev, rows=rows).view(-1)
+            fn = lambda: codec.quant_i8(x0, o[1], o[2])
+        elif op == "dequant_i8":
+            out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+            fn = lambda: codec.dequant_i8(wires[0][1], wires[0][2], out)
+        elif op == "dequant_accum_i8":
+            fn = lambda: codec.dequant_accum_i8([w[1] for w in wires], [w[2] for w in wires], o[1], o[2], None)
+        else:
+            xl = inputs.prefill_buffer(1, device=dev, rows=rows).view(-1)
+            fn = lambda: codec.ring_hop_i8(wires[0][1], wires[0][2], xl, o[1], o[2], None)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # hand the generators' temporaries back: only the op's buffers stay on the device
+    for _ in range(args.warmup + args.profile_launches):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_op": op, "rows": rows, "slice_rows": args.slice_rows, "warmup": args.warmup,
+                      "launches": args.profile_launches,
+                      "device_bytes_held": torch.cuda.memory_reserved(dev)}), flush=True)
+
+
 # ---------------------------------------------------------------- arms
 def workload_config(args, world: int) -> dict:
     """The `config` of both arms' JSON lines: the prefill step's workload."""
@@ -584,23 +784,31 @@ def run_bq(args, rank, world, local):
     torch.cuda.synchronize()
 
     # Timed region 1 (the reported value): K steps back to back, nothing between the
-    # launches, so consecutive kernels overlap their launch with the previous tail.
+    # launches of a step, so consecutive kernels overlap their launch with the previous
+    # tail; one event at each step boundary gives the per-step samples.
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    nvml = NvmlClocks(dev)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
+        nvml.mark_start()
         start.record()
         for k in range(args.steps):
             pipe.run()
+            step_ev[k].record()
         stop.record()
         torch.cuda.synchronize()
+        nvml.mark_stop()
         clk.mark_stop()
     barrier(world)
     ms_local = start.elapsed_time(stop)
     ms = max_over_ranks(ms_local, world)
     ms_per_step = ms / args.steps
+    step_ms = [start.elapsed_time(step_ev[0])] + [step_ev[k - 1].elapsed_time(step_ev[k])
+                                                   for k in range(1, args.steps)]
 
     # Timed region 2 (per-kernel durations for the roofline): the same K steps with a
     # CUDA event recorded after every launch on the launching stream.
@@ -636,8 +844,12 @@ def run_bq(args, rank, world, local):
         q = sorted(d["samples"])
         pct = {f"p{p}_us": round(q[min(len(q) - 1, int(p / 100 * len(q)))] * 1e3, 2) for p in (10, 50, 90)}
         kernels[name] = {"launches_per_step": d["launches"] // args.steps, "avg_us": round(avg_ms * 1e3, 2), **pct,
+                         "median_us": round(statistics.median(q) * 1e3, 2),
                          "bytes_per_launch": d["bytes"], "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                         "share": round(d["ms"] / ms_instr, 4)}
+                         "share": round(d["ms"] / ms_instr, 4),
+                         "samples_us": [round(t * 1e3, 2) for t in d["samples"][:RAW_SAMPLES]],
+                         "samples_note": f"launch durations in launch order, the first {min(RAW_SAMPLES, len(q))} "
+                                         f"of {len(q)}"}
     # the same kernels timed without the gaps that an event after every launch leaves:
     # each one's launches of a step, repeated, replayed from one CUDA graph
     if not args.no_next:
@@ -650,10 +862,11 @@ def run_bq(args, rank, world, local):
             def rotate(fns=fns, turn=turn):
                 fns[turn[0] % len(fns)][0]()
                 turn[0] += 1
-            gms = graph_ms(rotate, max(args.next_reps, len(fns) * 4))
+            gms, gsamples = graph_stats(rotate, max(args.next_reps, len(fns) * 4))
             gbs_g = fns[0][1] / (gms * 1e-3) / 1e9
             kernels[name].update({"graph_avg_us": round(gms * 1e3, 2), "graph_GB/s": round(gbs_g, 1),
-                                  "graph_frac": round(gbs_g / peak, 4)})
+                                  "graph_frac": round(gbs_g / peak, 4),
+                                  "graph_spread": spread(gsamples)})
     dominant = max(per, key=lambda k: per[k]["ms"])
     dk = kernels[dominant]
     traffic = None
@@ -713,12 +926,14 @@ def run_bq(args, rank, world, local):
                                            f"({nb1} algorithmic bytes, {dt1:.2f} s)"}}
 
     value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
-    clocks = clk.summary()
+    clocks = nvml.summary() or clk.summary()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config(args, world),
+        "step_median_ms": round(statistics.median(step_ms), 4),
+        "step_samples_ms": [round(t, 4) for t in step_ms[:RAW_SAMPLES]],
         "roofline": roofline, "kernels": kernels, "next_rows": next_rows, "configs": configs, "clocks": clocks,
         "e2e": e2e, "gpu_launches": nl * args.steps, "cpu_baseline": cpu,
         "device": torch.cuda.get_device_name(dev),
@@ -783,7 +998,14 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of CPU work for --impl reference")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="host threads for the oracle legs (0 = every core this process may use)")
+    ap.add_argument("--profile-op", choices=PROFILE_OPS, default=None,
+                    help="launch only this kernel (--warmup + --profile-launches times) on its own buffers, "
+                         "for profiler captures; prints no benchmark line")
+    ap.add_argument("--profile-launches", type=int, default=1)
     args = ap.parse_args(argv)
+    if args.profile_op:
+        run_profile_op(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
