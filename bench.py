@@ -681,7 +681,8 @@ def time_configs(args, peak):
 
 # ---------------------------------------------------------------- one kernel alone (profiling)
 PROFILE_OPS = ("quant_i8", "dequant_i8", "dequant_accum_i8", "ring_hop_i8", "quant_mx", "dequant_mx",
-               "quant_mx_slices", "dequant_accum_mx", "ring_hop_mx")
+               "quant_mx_slices", "quant_mx_f16", "quant_mx_tiled", "dequant_accum_mx", "ring_hop_mx",
+               "reduce_quant_i8", "reduce_quant_e4m3", "quant_e4m3", "dequant_e4m3")
 
 
 def run_profile_op(args):
@@ -695,23 +696,29 @@ def run_profile_op(args):
     dev = torch.device("cuda", 0)
     op, rows = args.profile_op, args.rows
     n = rows * HIDDEN
-    if op in ("quant_mx", "quant_mx_slices", "dequant_mx"):
-        sl = inputs.mx_slices_4096(device=dev, rows=args.slice_rows)
+    if op in ("quant_mx", "quant_mx_slices", "dequant_mx", "quant_mx_f16", "quant_mx_tiled"):
+        dt = torch.float16 if op == "quant_mx_f16" else torch.bfloat16
+        sl = inputs.mx_slices_4096(device=dev, rows=args.slice_rows, dtype=dt)
         q, s = codec.empty_mx(args.slice_rows, HIDDEN * N_SLICES, dev)
+        g_total = HIDDEN * N_SLICES // 32
+        tiled = torch.zeros((codec.mx_tiled_scale_bytes(args.slice_rows, g_total),), dtype=torch.uint8, device=dev)
         turn = [0]
 
         def one_slice():
             i = turn[0] % N_SLICES
             turn[0] += 1
             c0 = i * HIDDEN
-            codec.quant_mx(sl[i], q[:, c0:c0 + HIDDEN], s[:, c0 // 32:(c0 + HIDDEN) // 32])
+            if op == "quant_mx_tiled":
+                codec.quant_mx_tiled(sl[i], q[:, c0:c0 + HIDDEN], tiled, g_total, c0 // 32)
+            else:
+                codec.quant_mx(sl[i], q[:, c0:c0 + HIDDEN], s[:, c0 // 32:(c0 + HIDDEN) // 32])
         codec.quant_mx_slices(sl, q, s)
         if op == "dequant_mx":
             del sl
             out = torch.empty((args.slice_rows, HIDDEN * N_SLICES), dtype=torch.bfloat16, device=dev)
             fn = lambda: codec.dequant_mx(q, s, out)
         else:
-            fn = one_slice if op == "quant_mx" else (lambda: codec.quant_mx_slices(sl, q, s))
+            fn = (lambda: codec.quant_mx_slices(sl, q, s)) if op == "quant_mx_slices" else one_slice
     elif op in ("dequant_accum_mx", "ring_hop_mx"):
         nsrc = W_SRC if op == "dequant_accum_mx" else 1
         wires = [codec.empty_wire_mx(n, dev) for _ in range(nsrc)]
@@ -725,6 +732,24 @@ def run_profile_op(args):
         else:
             xl = inputs.prefill_buffer(1, device=dev, rows=rows).view(-1)
             fn = lambda: codec.ring_hop_mx(wires[0][1], wires[0][2], xl, o[1], o[2], None)
+    elif op in ("reduce_quant_i8", "reduce_quant_e4m3"):
+        xs = [inputs.prefill_buffer(w, device=dev, rows=rows).view(-1) for w in range(W_SRC)]
+        if op == "reduce_quant_i8":
+            o = codec.empty_wire_i8(n, dev)
+            fn = lambda: codec.reduce_quant_i8(xs, o[1], o[2], None)
+        else:
+            o = codec.empty_wire_e4m3(n, dev)
+            fn = lambda: codec.reduce_quant_e4m3(xs, o[1], o[2], None)
+    elif op in ("quant_e4m3", "dequant_e4m3"):
+        x0 = inputs.prefill_buffer(0, device=dev, rows=rows).view(-1)
+        o = codec.empty_wire_e4m3(n, dev)
+        codec.quant_e4m3(x0, o[1], o[2])
+        if op == "quant_e4m3":
+            fn = lambda: codec.quant_e4m3(x0, o[1], o[2])
+        else:
+            del x0
+            out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+            fn = lambda: codec.dequant_e4m3(o[1], o[2], out)
     else:
         nsrc = {"quant_i8": 0, "dequant_i8": 1, "dequant_accum_i8": W_SRC, "ring_hop_i8": 1}[op]
         wires = [codec.empty_wire_i8(n, dev) for _ in range(nsrc)]
