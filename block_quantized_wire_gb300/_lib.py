@@ -19,7 +19,7 @@ _lib = None
 ABI_VERSION = 5
 BQ_OK = 0
 STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_ALIAS",
-                5: "BQ_ERR_CUDA"}
+                5: "BQ_ERR_CUDA", 6: "BQ_ERR_UNSUPPORTED"}
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -45,6 +45,9 @@ _PROTOS = {
     "bq_reduce_quant_e4m3": ([_P, ctypes.c_int, _I64, _P, _P, _P, _P], ctypes.c_int),
     "bq_take_wait_timeouts": ([_P], ctypes.c_int),
     "bq_take_wait_unlanded": ([_P], ctypes.c_int),
+    "bq_take_index_errors": ([_P], ctypes.c_int),
+    "bq_debug_build": ([], ctypes.c_int),
+    "bq_selftest_index_check": ([_P, _I64, _P], ctypes.c_int),
     "bq_selftest_wait_timeout": ([_P], ctypes.c_int),
 }
 

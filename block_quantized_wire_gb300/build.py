@@ -26,6 +26,11 @@ OBJDIR = os.path.join(PKG, "_build")
 ALT_LIB = os.path.join(PKG, "libbq_alt.so")
 ALT_OBJDIR = os.path.join(PKG, "_build_alt")
 ALT_FLAGS = ["-DBQ_ACCUM_WIDE=0", "-DBQ_QUANT_WIDE=0", "-DBQ_HOP_WIDE=0", "-DBQ_MX_WIDE=0", "-DBQ_WIDE_V8=0"]
+# The debug build: every kernel checks each global access against the buffers its
+# arguments describe and counts (instead of performing) an access outside them.
+DEBUG_LIB = os.path.join(PKG, "libbq_debug.so")
+DEBUG_OBJDIR = os.path.join(PKG, "_build_debug")
+DEBUG_FLAGS = ["-DBQ_DEBUG=1"]
 
 SOURCES = ["bq_api.cu", "bq_i8.cu", "bq_mx.cu", "bq_mx_wire.cu", "bq_e4m3.cu"]
 HEADERS = ["bq_device.cuh", "bq_launch.h", "bq_chunks.cuh"]
@@ -95,6 +100,11 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=(), li
 def build_alt_library(force: bool = False, verbose: bool = False) -> str:
     """Build libbq_alt.so: the sources with ALT_FLAGS."""
     return build_library(force, verbose, ALT_FLAGS, ALT_LIB, ALT_OBJDIR)
+
+
+def build_debug_library(force: bool = False, verbose: bool = False) -> str:
+    """Build libbq_debug.so: the sources with DEBUG_FLAGS."""
+    return build_library(force, verbose, DEBUG_FLAGS, DEBUG_LIB, DEBUG_OBJDIR)
 
 
 def _build_locked(verbose: bool, extra_flags, lib: str, objdir: str) -> str:

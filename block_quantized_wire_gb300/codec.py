@@ -352,6 +352,25 @@ def take_wait_timeouts() -> int:
     return int(n.value)
 
 
+def take_index_errors() -> int:
+    """Accesses a debug build's checks declined on the current device since the previous
+    call (always 0 in the default build)."""
+    n = ctypes.c_int64(0)
+    check("bq_take_index_errors", load().bq_take_index_errors(ctypes.byref(n)))
+    return int(n.value)
+
+
+def debug_build() -> bool:
+    """True if the loaded library is the debug build (BQ_DEBUG=1)."""
+    return bool(load().bq_debug_build())
+
+
+def selftest_index_check(buf: torch.Tensor, stream=None) -> None:
+    """Debug build: one deliberately declined load against a 1 KB device buffer."""
+    check("bq_selftest_index_check", load().bq_selftest_index_check(_flat(buf, torch.uint8, "buf"), buf.numel(),
+                                                                    _stream(stream)))
+
+
 def take_wait_unlanded() -> int:
     """Bulk copies that had not landed within the limit after an abandoned wait, since
     the previous call (each may have written a finished block's shared memory)."""

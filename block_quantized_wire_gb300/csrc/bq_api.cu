@@ -7,6 +7,10 @@
 #include "bq.h"
 #include "bq_launch.h"
 
+#ifndef BQ_DEBUG
+#define BQ_DEBUG 0
+#endif
+
 namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -112,6 +116,7 @@ const char *bq_status_string(int status)
     case BQ_ERR_ALIGN: return "pointer or leading dimension breaks the alignment rules";
     case BQ_ERR_ALIAS: return "an output overlaps an input or another output";
     case BQ_ERR_CUDA: return "the CUDA runtime reported an error for the launch";
+    case BQ_ERR_UNSUPPORTED: return "the call needs the debug build (BQ_DEBUG=1)";
     default: return "unknown status";
     }
 }
@@ -424,13 +429,13 @@ bq_status bq_reduce_quant_e4m3(const void *const *x_srcs, int W, int64_t n, uint
 }  // extern "C"
 
 namespace {
-// Growth of the current device's bounded-wait counter `which` (0: abandoned waits,
-// 1: copies that did not land after one) since the previous call for it. The device
-// counters only grow; the last totals seen are kept per device here, and they are
-// advanced only after every translation unit's counters were read.
+// Growth of the current device's counter `which` (0: abandoned waits, 1: copies that
+// did not land after one, 2: accesses a debug build declined) since the previous call
+// for it. The device counters only grow; the last totals seen are kept per device here,
+// and they are advanced only after every translation unit's counters were read.
 constexpr int kMaxDevices = 64;
 std::mutex g_seen_mu;
-unsigned long long g_seen[kMaxDevices][2];
+unsigned long long g_seen[kMaxDevices][3];
 
 bq_status take_wait_counter(int which, int64_t *count)
 {
@@ -440,7 +445,7 @@ bq_status take_wait_counter(int which, int64_t *count)
     unsigned long long total = 0;
     for (auto read : {bqk::read_wait_counters_i8, bqk::read_wait_counters_mx_wire, bqk::read_wait_counters_mx,
                       bqk::read_wait_counters_e4m3}) {
-        unsigned long long v[2] = {0, 0};
+        unsigned long long v[3] = {0, 0, 0};
         if (read(v) != cudaSuccess) return BQ_ERR_CUDA;
         total += v[which];
     }
@@ -456,6 +461,19 @@ extern "C" {
 bq_status bq_take_wait_timeouts(int64_t *count) { return take_wait_counter(0, count); }
 
 bq_status bq_take_wait_unlanded(int64_t *count) { return take_wait_counter(1, count); }
+
+bq_status bq_take_index_errors(int64_t *count) { return take_wait_counter(2, count); }
+
+int bq_debug_build(void) { return BQ_DEBUG; }
+
+bq_status bq_selftest_index_check(void *buf, int64_t bytes, cudaStream_t stream)
+{
+    if (!BQ_DEBUG) return BQ_ERR_UNSUPPORTED;
+    if (!buf) return BQ_ERR_NULL;
+    if (bytes < 1024) return BQ_ERR_SHAPE;
+    if (!aligned(buf, 16)) return BQ_ERR_ALIGN;
+    return from_cuda(bqk::launch_index_selftest(buf, stream));
+}
 
 bq_status bq_selftest_wait_timeout(cudaStream_t stream) { return from_cuda(bqk::launch_wait_selftest(stream)); }
 

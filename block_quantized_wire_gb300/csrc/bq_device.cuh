@@ -22,6 +22,114 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSegs = 4;                      // segments per warp iteration
 constexpr int kChunkBlocks = 2 * kSegs;       // 128-value blocks per warp iteration
 
+// ---------------------------------------------------------------- debug build
+// With -DBQ_DEBUG=1 (libbq_debug.so) every global access of a codec kernel is checked
+// against the buffers the kernel was given. At entry each kernel lists its buffers' byte
+// ranges from its own arguments (inputs read-only, outputs writable); a load, store or
+// bulk copy whose bytes do not lie inside one listed range of the right kind is not
+// performed (a load yields zeros) and is counted in g_index_errors, which the host reads
+// through bq_take_index_errors. Nothing traps. In the default build the checks are the
+// constant true and the listing is empty, so the kernels' code is unchanged.
+#ifndef BQ_DEBUG
+#define BQ_DEBUG 0
+#endif
+static __device__ unsigned long long g_index_errors;
+constexpr int kDbgMaxRanges = 2 * kMaxSources + 8;
+
+#if BQ_DEBUG
+struct DbgRanges {
+    unsigned long long lo[kDbgMaxRanges], hi[kDbgMaxRanges], writable;
+    int n;
+};
+__device__ __forceinline__ DbgRanges &dbg_ranges()
+{
+    __shared__ DbgRanges r;
+    return r;
+}
+#endif
+
+// Start of a kernel's buffer list (every thread calls it).
+__device__ __forceinline__ void dbg_begin()
+{
+#if BQ_DEBUG
+    if (threadIdx.x == 0) {
+        dbg_ranges().n = 0;
+        dbg_ranges().writable = 0;
+    }
+#endif
+}
+
+// One buffer of `bytes` bytes at p (thread 0 records it; the others ignore the call).
+__device__ __forceinline__ void dbg_allow(const void *p, int64_t bytes, bool writable)
+{
+#if BQ_DEBUG
+    DbgRanges &r = dbg_ranges();
+    if (threadIdx.x == 0 && bytes > 0 && r.n < kDbgMaxRanges) {
+        r.lo[r.n] = reinterpret_cast<unsigned long long>(p);
+        r.hi[r.n] = r.lo[r.n] + static_cast<unsigned long long>(bytes);
+        if (writable) r.writable |= 1ull << r.n;
+        r.n++;
+    }
+#else
+    (void)p, (void)bytes, (void)writable;
+#endif
+}
+
+// A row-major strided buffer: rows of row_bytes, ld_bytes apart.
+__device__ __forceinline__ void dbg_allow_2d(const void *p, int64_t rows, int64_t row_bytes, int64_t ld_bytes,
+                                             bool writable)
+{
+    if (rows > 0) dbg_allow(p, (rows - 1) * ld_bytes + row_bytes, writable);
+}
+
+// End of the list: the ranges are visible to every thread of the CTA.
+__device__ __forceinline__ void dbg_ready()
+{
+#if BQ_DEBUG
+    __syncthreads();
+#endif
+}
+
+// True if [p, p + bytes) lies inside one listed range (a writable one for a store).
+__device__ __forceinline__ bool dbg_ok(const void *p, int64_t bytes, bool write)
+{
+#if BQ_DEBUG
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p), b = a + static_cast<unsigned long long>(bytes);
+    const DbgRanges &r = dbg_ranges();
+    for (int i = 0; i < r.n; i++)
+        if (a >= r.lo[i] && b <= r.hi[i] && (!write || ((r.writable >> i) & 1ull))) return true;
+    atomicAdd(&g_index_errors, 1ull);
+    return false;
+#else
+    (void)p, (void)bytes, (void)write;
+    return true;
+#endif
+}
+
+// Listing helpers. A flat wire of 128 * nblk values: the payload (128 bytes per block)
+// and the scale words (4 bytes per block); a BF16 tensor of 128 * nblk values.
+__device__ __forceinline__ void dbg_wire(const void *q, const void *s, int64_t nblk, bool writable)
+{
+    dbg_allow(q, 128 * nblk, writable);
+    dbg_allow(s, 4 * nblk, writable);
+}
+
+__device__ __forceinline__ void dbg_bf16(const void *x, int64_t nblk, bool writable)
+{
+    dbg_allow(x, 256 * nblk, writable);
+}
+
+template <class TQ, class TS>
+__device__ __forceinline__ void dbg_sources(const WireList<TQ, TS> &src, int nsrc, int64_t nblk)
+{
+    for (int i = 0; i < nsrc && i < kMaxSources; i++) dbg_wire(src.q[i], src.s[i], nblk, false);
+}
+
+__device__ __forceinline__ void dbg_sources(const Bf16List &src, int nsrc, int64_t nblk)
+{
+    for (int i = 0; i < nsrc && i < kMaxSources; i++) dbg_bf16(src.x[i], nblk, false);
+}
+
 // ---------------------------------------------------------------- launch ordering
 // First statement of every codec kernel (see launch_kernel in bq_launch.h): wait for
 // the previous grid's completion and memory, then let the next grid start launching.
@@ -44,11 +152,12 @@ static __device__ unsigned long long g_wait_timeouts;
 static __device__ unsigned long long g_wait_unlanded;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
-// Host side: this translation unit's two counters, {timeouts, unlanded}.
-static inline cudaError_t read_wait_counters(unsigned long long (&v)[2])
+// Host side: this translation unit's counters, {timeouts, unlanded, index errors}.
+static inline cudaError_t read_wait_counters(unsigned long long (&v)[3])
 {
     if (cudaError_t e = cudaMemcpyFromSymbol(&v[0], g_wait_timeouts, sizeof v[0])) return e;
-    return cudaMemcpyFromSymbol(&v[1], g_wait_unlanded, sizeof v[1]);
+    if (cudaError_t e = cudaMemcpyFromSymbol(&v[1], g_wait_unlanded, sizeof v[1])) return e;
+    return cudaMemcpyFromSymbol(&v[2], g_index_errors, sizeof v[2]);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -71,6 +180,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
+    if (!dbg_ok(src, bytes, false)) return;  // the stage's barrier then runs out of time, counted too
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
@@ -115,6 +225,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 // Inputs are read once: non-coherent path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 {
+    if (!dbg_ok(p, 16, false)) return make_uint4(0, 0, 0, 0);
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
@@ -124,6 +235,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 
 __device__ __forceinline__ uint2 ld_stream_v2(const void *p)
 {
+    if (!dbg_ok(p, 8, false)) return make_uint2(0, 0);
     uint2 r;
     asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
     return r;
@@ -134,6 +246,10 @@ __device__ __forceinline__ uint2 ld_stream_v2(const void *p)
 // host and take 16-byte accesses otherwise.
 __device__ __forceinline__ void ld_stream_v8(const void *p, uint4 &a, uint4 &b)
 {
+    if (!dbg_ok(p, 32, false)) {
+        a = b = make_uint4(0, 0, 0, 0);
+        return;
+    }
     asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
         : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
         : "l"(p));
@@ -141,6 +257,7 @@ __device__ __forceinline__ void ld_stream_v8(const void *p, uint4 &a, uint4 &b)
 
 __device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
 {
+    if (!dbg_ok(p, 4, false)) return 0u;
     uint32_t r;
     asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
@@ -148,6 +265,7 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
 
 __device__ __forceinline__ void st_v4(void *p, uint4 v)
 {
+    if (!dbg_ok(p, 16, true)) return;
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
@@ -155,6 +273,7 @@ __device__ __forceinline__ void st_v4(void *p, uint4 v)
 
 __device__ __forceinline__ void st_v8(void *p, uint4 a, uint4 b)
 {
+    if (!dbg_ok(p, 32, true)) return;
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
                  "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
                  : "memory");
@@ -162,11 +281,13 @@ __device__ __forceinline__ void st_v8(void *p, uint4 a, uint4 b)
 
 __device__ __forceinline__ void st_v2(void *p, uint2 v)
 {
+    if (!dbg_ok(p, 8, true)) return;
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 __device__ __forceinline__ void st_u32(void *p, uint32_t v)
 {
+    if (!dbg_ok(p, 4, true)) return;
     asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 

@@ -44,7 +44,7 @@ __device__ __forceinline__ void requant_e4m3_chunk(const Vals &vals, int64_t e0,
             if (kOut) st_v4(out + e0 + 256 * j, e4m3_materialize8(codes, bj.s));
         }
     }
-    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) s[b0 + lane] = mine.s;
+    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk) && dbg_ok(s + b0 + lane, 4, true)) s[b0 + lane] = mine.s;
 }
 
 struct E4m3Codec {
@@ -71,6 +71,10 @@ __global__ void __launch_bounds__(kThreads, BQ_QUANT_E4M3_MIN_CTAS)
 quant_e4m3_kernel(const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_ready();
     const QuantOp<E4m3Codec, SEGS, true> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -81,6 +85,10 @@ dequant_e4m3_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s, 
                     uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q, s, nblk, false);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const DequantOp<E4m3Codec, SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<true>(op, nblk, 2 * SEGS);
 }
@@ -91,6 +99,11 @@ reduce_quant_e4m3_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t
                          float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const ReduceQuantOp<E4m3Codec, SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -147,6 +160,6 @@ cudaError_t launch_reduce_quant_e4m3(const Bf16List &src, int W, int64_t nblk, u
     }
 }
 
-cudaError_t read_wait_counters_e4m3(unsigned long long (&v)[2]) { return read_wait_counters(v); }
+cudaError_t read_wait_counters_e4m3(unsigned long long (&v)[3]) { return read_wait_counters(v); }
 
 }  // namespace bqk

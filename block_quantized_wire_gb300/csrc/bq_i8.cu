@@ -45,7 +45,7 @@ __device__ __forceinline__ void requant_chunk(const Vals &vals, int64_t e0, int6
             if (kOut) st_v4(out + e0 + 256 * j, i8_materialize_words(w, bj.s));
         }
     }
-    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk)) s[b0 + lane] = mine.s;
+    if (lane < 2 * SEGS && (!kTail || b0 + lane < nblk) && dbg_ok(s + b0 + lane, 4, true)) s[b0 + lane] = mine.s;
 }
 
 // Block-INT8 codec policy for the shared reductions: d = fl(q * s) per element
@@ -92,6 +92,10 @@ __global__ void __launch_bounds__(kThreads, BQ_QUANT_MIN_CTAS)
 quant_i8_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_ready();
     const QuantI8<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -101,6 +105,10 @@ __global__ void __launch_bounds__(kThreads)
 quant_i8_staged_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_ready();
     extern __shared__ __align__(128) unsigned char smem[];
     const QuantI8<SEGS> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<QuantI8<SEGS>, STAGES>());
@@ -115,6 +123,10 @@ __global__ void __launch_bounds__(kThreads)
 dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q, s, nblk, false);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const DequantI8<SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<true>(op, nblk, 2 * SEGS);
 }
@@ -133,6 +145,11 @@ accum_i8_staged_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t
                        float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     extern __shared__ __align__(128) unsigned char smem[];
     const AccumI8<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_staged<STAGES>(op, nblk, 2 * SEGS,
@@ -145,6 +162,11 @@ accum_i8_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, 
                 uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const AccumI8<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -216,7 +238,7 @@ __device__ __forceinline__ void requant_wide(const float2 (&v)[2][2][4], int64_t
             }
         }
     }
-    if (lane < 8 && (!kTail || b0 + lane < nblk)) s[b0 + lane] = sb.s;
+    if (lane < 8 && (!kTail || b0 + lane < nblk) && dbg_ok(s + b0 + lane, 4, true)) s[b0 + lane] = sb.s;
 }
 
 template <bool kV8>
@@ -414,6 +436,12 @@ ring_hop_i8_wide_kernel(const int8_t *__restrict__ q_in, const float *__restrict
                         uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q_in, s_in, nblk, false);
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const HopWideI8<kOut, kV8> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 8);
 }
@@ -431,6 +459,11 @@ accum_i8_wide_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t n
                      float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const AccumWideI8<W, kOut, kMore, kV8> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 8);
 }
@@ -440,6 +473,10 @@ __global__ void __launch_bounds__(kThreads, BQ_QUANT_MIN_CTAS)
 quant_i8_wide_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_ready();
     const QuantWideI8<kV8> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 8);
 }
@@ -455,6 +492,12 @@ ring_hop_i8_staged_kernel(const int8_t *__restrict__ q_in, const float *__restri
                           float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q_in, s_in, nblk, false);
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     extern __shared__ __align__(128) unsigned char smem[];
     const HopI8<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<HopI8<SEGS, kOut>, STAGES>());
@@ -466,6 +509,12 @@ ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_
                    int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q_in, s_in, nblk, false);
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const HopI8<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -477,6 +526,11 @@ reduce_quant_i8_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t n
                        float *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const ReduceQuantOp<I8Codec, SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -590,13 +644,33 @@ __global__ void wait_selftest_kernel()
 }
 }  // namespace
 
+// Debug build: the kernel lists only the first 256 bytes of a 1 KB caller buffer and
+// then loads 16 bytes at byte 512, which the check declines (and counts) instead of
+// performing. The load would stay inside the caller's buffer in any case.
+__global__ void index_selftest_kernel(unsigned char *buf)
+{
+    dbg_begin();
+    dbg_allow(buf, 256, true);
+    dbg_ready();
+    if (threadIdx.x == 0) {
+        const uint4 v = ld_stream_v4(buf + 512);
+        st_v4(buf, v);  // inside the listed range: performed (zeros from the declined load)
+    }
+}
+
+cudaError_t launch_index_selftest(void *buf, cudaStream_t st)
+{
+    index_selftest_kernel<<<1, 32, 0, st>>>(static_cast<unsigned char *>(buf));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(cudaStream_t st)
 {
     wait_selftest_kernel<<<1, 32, 0, st>>>();
     return cudaGetLastError();
 }
 
-cudaError_t read_wait_counters_i8(unsigned long long (&v)[2]) { return read_wait_counters(v); }
+cudaError_t read_wait_counters_i8(unsigned long long (&v)[3]) { return read_wait_counters(v); }
 
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
 {

@@ -108,12 +108,14 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, A
 // the device queries, if any.
 cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem = 0);
 
-// Each kernel translation unit's bounded-wait counters {timeouts, unlanded} (see
+// Each kernel translation unit's counters {wait timeouts, unlanded copies, debug index errors} (see
 // g_wait_timeouts in bq_device.cuh): totals since the library was loaded, never reset.
-cudaError_t read_wait_counters_i8(unsigned long long (&v)[2]);
-cudaError_t read_wait_counters_mx_wire(unsigned long long (&v)[2]);
-cudaError_t read_wait_counters_mx(unsigned long long (&v)[2]);
-cudaError_t read_wait_counters_e4m3(unsigned long long (&v)[2]);
+cudaError_t read_wait_counters_i8(unsigned long long (&v)[3]);
+cudaError_t read_wait_counters_mx_wire(unsigned long long (&v)[3]);
+cudaError_t read_wait_counters_mx(unsigned long long (&v)[3]);
+cudaError_t read_wait_counters_e4m3(unsigned long long (&v)[3]);
 cudaError_t launch_wait_selftest(cudaStream_t st);
+// Debug build: one listed 256-byte range of buf and one load at byte 512 (declined).
+cudaError_t launch_index_selftest(void *buf, cudaStream_t st);
 
 }  // namespace bqk

@@ -230,6 +230,17 @@ quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64
                 int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s, int64_t c0)
 {
     pdl_begin();
+    dbg_begin();
+    if (bpr > 0) {
+        const int64_t rows = nblk / bpr;
+        dbg_allow_2d(x, rows, 256 * bpr, 2 * ld_x, false);
+        dbg_allow_2d(q, rows, 128 * bpr, ld_q, true);
+        if (kTiled)
+            dbg_allow(s, (rows + 127) / 128 * ld_s * 512, true);  // ld_s: tiles per tile row
+        else
+            dbg_allow_2d(s, rows, 4 * bpr, ld_s, true);
+    }
+    dbg_ready();
     quant_mx_matrix<kF16, kTiled>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, blockIdx.x, gridDim.x);
 }
 
@@ -243,6 +254,14 @@ quant_mx_slices_kernel(const __grid_constant__ MxSliceList sl, int64_t rows, uin
                        uint8_t *__restrict__ s, int64_t ld_s)
 {
     pdl_begin();
+    dbg_begin();
+    for (int i = 0; i < sl.n; i++) dbg_allow_2d(sl.x[i], rows, 256 * sl.bpr[i], 2 * sl.ld_x[i], false);
+    if (sl.n > 0) {
+        const int64_t blocks = sl.cb0[sl.n - 1] + sl.bpr[sl.n - 1];
+        dbg_allow_2d(q, rows, 128 * blocks, ld_q, true);
+        dbg_allow_2d(s, rows, 4 * blocks, ld_s, true);
+    }
+    dbg_ready();
     int i = 0;
     while (i + 1 < sl.n && static_cast<int>(blockIdx.x) >= sl.cta0[i + 1]) ++i;
     const int64_t bpr = sl.bpr[i];
@@ -300,6 +319,14 @@ dequant_mx_kernel(const uint8_t *__restrict__ q, int64_t ld_q, const uint8_t *__
                   int64_t bpr, int64_t nblk, uint16_t *__restrict__ out, int64_t ld_out)
 {
     pdl_begin();
+    dbg_begin();
+    if (bpr > 0) {
+        const int64_t rows = nblk / bpr;
+        dbg_allow_2d(q, rows, 128 * bpr, ld_q, false);
+        dbg_allow_2d(s, rows, 4 * bpr, ld_s, false);
+        dbg_allow_2d(out, rows, 256 * bpr, 2 * ld_out, true);
+    }
+    dbg_ready();
     const int lane = threadIdx.x & 31;
     constexpr int CB = 2 * SEGS;
     const int64_t nfull = nblk / CB;
@@ -401,6 +428,6 @@ cudaError_t launch_dequant_mx(const uint8_t *q, int64_t ld_q, const uint8_t *s, 
     return launch_kernel(dequant_mx_kernel<kSegsDequantMx>, grid, st, q, ld_q, s, ld_s, bpr, nblk, out, ld_out);
 }
 
-cudaError_t read_wait_counters_mx(unsigned long long (&v)[2]) { return read_wait_counters(v); }
+cudaError_t read_wait_counters_mx(unsigned long long (&v)[3]) { return read_wait_counters(v); }
 
 }  // namespace bqk

@@ -62,7 +62,9 @@ __device__ __forceinline__ void requant_mx_chunk(const Vals &vals, int64_t e0, i
     uint32_t word = e << (8 * (lane & 3));
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
-    if ((lane & 3) == 0 && (lane >> 2) < 2 * SEGS && (!kTail || b0 + (lane >> 2) < nblk)) s[b0 + (lane >> 2)] = word;
+    if ((lane & 3) == 0 && (lane >> 2) < 2 * SEGS && (!kTail || b0 + (lane >> 2) < nblk) &&
+        dbg_ok(s + b0 + (lane >> 2), 4, true))
+        s[b0 + (lane >> 2)] = word;
 }
 
 // MXFP8 codec policy for the shared reductions.
@@ -149,7 +151,8 @@ __device__ __forceinline__ void requant_mx_wide(const float2 (&v)[2][2][4], int6
     uint32_t word = e << (8 * (lane & 3));
     word |= __shfl_xor_sync(kFull, word, 1);
     word |= __shfl_xor_sync(kFull, word, 2);
-    if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk)) s[b0 + (lane >> 2)] = word;
+    if ((lane & 3) == 0 && (!kTail || b0 + (lane >> 2) < nblk) && dbg_ok(s + b0 + (lane >> 2), 4, true))
+        s[b0 + (lane >> 2)] = word;
 }
 
 template <int W, bool kOut, bool kMore, bool kV8>
@@ -301,6 +304,11 @@ accum_mx_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t nblk
                 uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const AccumMx<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -311,6 +319,11 @@ accum_mx_staged_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64
                        uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     extern __shared__ __align__(128) unsigned char smem[];
     const AccumMx<SEGS, W, kOut, kMore> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_staged<STAGES>(op, nblk, 2 * SEGS,
@@ -323,6 +336,12 @@ ring_hop_mx_kernel(const uint8_t *__restrict__ q_in, const uint32_t *__restrict_
                    int64_t nblk, uint8_t *__restrict__ q, uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q_in, s_in, nblk, false);
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const HopMx<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
 }
@@ -334,6 +353,12 @@ ring_hop_mx_staged_kernel(const uint8_t *__restrict__ q_in, const uint32_t *__re
                           uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q_in, s_in, nblk, false);
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     extern __shared__ __align__(128) unsigned char smem[];
     const HopMx<SEGS, kOut> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<HopMx<SEGS, kOut>, STAGES>());
@@ -345,6 +370,11 @@ accum_mx_wide_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t
                      uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const AccumWideMx<W, kOut, kMore, kV8> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 8);
 }
@@ -356,6 +386,12 @@ ring_hop_mx_wide_kernel(const uint8_t *__restrict__ q_in, const uint32_t *__rest
                         uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
     pdl_begin();
+    dbg_begin();
+    dbg_wire(q_in, s_in, nblk, false);
+    dbg_bf16(x, nblk, false);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
     const HopWideMx<kOut, kV8> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 8);
 }
@@ -465,6 +501,6 @@ cudaError_t launch_ring_hop_mx(const uint8_t *q_in, const uint32_t *s_in, const 
     return launch_hop_mx_stages<kStagesHopMx, false>(q_in, s_in, x, nblk, q, s, nullptr, st);
 }
 
-cudaError_t read_wait_counters_mx_wire(unsigned long long (&v)[2]) { return read_wait_counters(v); }
+cudaError_t read_wait_counters_mx_wire(unsigned long long (&v)[3]) { return read_wait_counters(v); }
 
 }  // namespace bqk

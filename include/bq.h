@@ -108,7 +108,8 @@ typedef enum {
                          [1, BQ_MAX_W], or a leading dimension too small */
     BQ_ERR_ALIGN = 3, /* a pointer or leading dimension breaks the alignment rules */
     BQ_ERR_ALIAS = 4, /* an output overlaps an input or another output */
-    BQ_ERR_CUDA = 5   /* the CUDA runtime reported an error for this call's launch */
+    BQ_ERR_CUDA = 5,  /* the CUDA runtime reported an error for this call's launch */
+    BQ_ERR_UNSUPPORTED = 6 /* the call exists only in the debug build (bq_selftest_index_check) */
 } bq_status;
 
 /* BQ_ABI_VERSION of the loaded library. */
@@ -313,6 +314,26 @@ BQ_API bq_status bq_take_wait_timeouts(int64_t *count);
  * 0 unless bq_take_wait_timeouts reported a timeout. Same conventions as
  * bq_take_wait_timeouts. */
 BQ_API bq_status bq_take_wait_unlanded(int64_t *count);
+
+/* The debug build (libbq_debug.so, compiled with BQ_DEBUG=1; no counterpart on the
+ * pages, it is this library's own bounds checking): every kernel lists the byte ranges
+ * of the buffers its arguments describe, inputs read-only and outputs writable, and each
+ * global load, store and bulk copy is checked against them. An access outside every
+ * listed range (or a store into an input) is not performed, a load yielding zeros, and
+ * is counted; nothing traps. bq_take_index_errors returns the growth of that count on
+ * the current device since its previous call (always 0 in the default build, whose
+ * kernels contain no checks). Same conventions as bq_take_wait_timeouts. */
+BQ_API bq_status bq_take_index_errors(int64_t *count);
+
+/* 1 in the debug build, 0 in the default build. */
+BQ_API int bq_debug_build(void);
+
+/* Debug build only: one kernel lists the first 256 bytes of buf as its buffer and then
+ * loads 16 bytes at byte 512, which the check must decline and count: the next
+ * bq_take_index_errors returns 1. buf: device memory of at least 1024 bytes, 16-byte
+ * aligned (its first 16 bytes are overwritten with zeros). BQ_ERR_UNSUPPORTED in the
+ * default build, which launches nothing. */
+BQ_API bq_status bq_selftest_index_check(void *buf, int64_t bytes, cudaStream_t stream);
 
 /* Self-test of the bounded wait: one warp waits on a barrier that nothing completes,
  * with a 20 ms limit, so the count read by bq_take_wait_timeouts grows by exactly one.

@@ -29,7 +29,8 @@ def test_header_declares_the_calls():
                  "bq_dequant_mx", "bq_dequant_accum_mx", "bq_ring_hop_mx", "bq_quant_mx_f16", "bq_reduce_quant_i8",
                  "bq_quant_e4m3", "bq_dequant_e4m3", "bq_reduce_quant_e4m3", "bq_quant_mx_tiled", "bq_quant_mx_slices",
                  "bq_mx_tiled_scale_bytes", "bq_wire_bytes", "bq_status_string",
-                 "bq_abi_version", "bq_take_wait_timeouts", "bq_take_wait_unlanded", "bq_selftest_wait_timeout"):
+                 "bq_abi_version", "bq_take_wait_timeouts", "bq_take_wait_unlanded", "bq_selftest_wait_timeout",
+                 "bq_take_index_errors", "bq_debug_build", "bq_selftest_index_check"):
         assert want in names
 
 
@@ -351,3 +352,11 @@ def test_alternative_build_flags_name_existing_switches():
         m = re.fullmatch(r"-D(BQ_[A-Z0-9_]+)=0", flag)
         assert m, flag
         assert f"#ifndef {m.group(1)}" in src and f"#define {m.group(1)} 1" in src, flag
+
+
+def test_default_build_has_no_debug_checks(bq_lib):
+    # the default build compiles the access checks away and refuses the debug self-test
+    # before touching the device
+    assert bq_lib.bq_debug_build() == 0
+    assert bq_lib.bq_selftest_index_check(None, 0, None) == 6  # BQ_ERR_UNSUPPORTED
+    assert bq_lib.bq_status_string(6).decode().startswith("the call needs the debug build")
