@@ -250,7 +250,10 @@ BQ_API bq_status bq_quant_mx_tiled(const void *x, int x_is_f16, int64_t rows, in
  *                    (written), as in bq_quant_mx, for the total of the slices'
  *                    columns; offset them for a batch that starts at another
  *                    128-column-aligned column
- * Slices may overlap one another; the outputs may overlap none of them. */
+ * Slices may overlap one another; the outputs may overlap none of them. Errors as
+ * bq_quant_mx (every slice is checked before the launch), plus BQ_ERR_SHAPE for nslices
+ * outside 1..BQ_MAX_SLICES. The slice list is copied into the launch's parameters:
+ * nothing is allocated, and the host array may be reused as soon as the call returns. */
 typedef struct bq_mx_slice {
     const void *x;
     int64_t cols;

@@ -241,3 +241,24 @@ def test_slices_in_one_call_staged_workload():
     q_ref, s_ref = oracle.quant_mx(bits(cat))
     assert_same(q[pick], q_ref, "E4M3 codes")
     assert_same(s[pick], s_ref, "E8M0 scales")
+
+
+def test_slices_in_one_call_graph_replay_is_bit_identical():
+    # stream-ordered and allocation-free: the call captures into a CUDA graph, and a
+    # replay writes the bytes of the eager call
+    slices = inputs.mx_slices_4096(rows=256, n_slices=3)
+    rows, cols = slices[0].shape
+    q, s = codec.empty_mx(rows, 3 * cols)
+    codec.quant_mx_slices(slices, q, s)
+    torch.cuda.synchronize()
+    q_eager, s_eager = q.clone(), s.clone()
+    q.fill_(0)
+    s.fill_(0)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        codec.quant_mx_slices(slices, q, s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(q, q_eager) and torch.equal(s, s_eager)
