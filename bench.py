@@ -501,6 +501,61 @@ def oracle_sample(pipe_inputs, rows: int, slice_rows: int, threads: int = 1):
     return time.perf_counter() - t0, nbytes
 
 
+def oracle_parity(pipe, rows: int, slice_rows: int) -> dict:
+    """Part of the CPU-oracle leg: the step's GPU outputs on the first `rows` rows of every
+    INT8 buffer and `slice_rows` rows of every MX slice, compared byte for byte with the
+    oracle's outputs for the same input bits (blocks and groups are independent, so the
+    first rows of an output depend only on the first rows of its inputs)."""
+    import numpy as np
+
+    import oracle
+    from block_quantized_wire_gb300.inputs import bf16_bits
+
+    def same(dev, want):
+        got = dev.detach().contiguous().cpu()
+        got = got.view(torch.int16) if got.dtype == torch.bfloat16 else got
+        return bool(np.array_equal(got.numpy().reshape(-1).view(np.uint8), np.asarray(want).reshape(-1).view(np.uint8)))
+
+    pipe.run()  # the later sections reuse the step's output buffers: one more step restores them
+    torch.cuda.synchronize()
+    n = rows * HIDDEN
+    xb = [bf16_bits(x[:rows]).reshape(-1) for x in pipe.xs]
+    qs = [oracle.quant_i8(b) for b in xb]
+    qa, sa, _ = oracle.dequant_accum_i8([q for q, _ in qs], [s for _, s in qs], materialize=False)
+    qh, sh, _ = oracle.ring_hop_i8(qs[0][0], qs[0][1], xb[1])
+    ok = {"quant_i8": all(same(pipe.wires[w][1][:n], qs[w][0]) and same(pipe.wires[w][2][:n // 128], qs[w][1])
+                          for w in range(W_SRC)),
+          "dequant_accum_i8": same(pipe.acc[1][:n], qa) and same(pipe.acc[2][:n // 128], sa),
+          "dequant_i8": same(pipe.out.view(-1)[:n], oracle.dequant_i8(qa, sa)),
+          "ring_hop_i8": same(pipe.hop[1][:n], qh) and same(pipe.hop[2][:n // 128], sh)}
+    C = HIDDEN * N_SLICES
+    qb = np.empty((slice_rows, C), np.uint8)
+    sbuf = np.empty((slice_rows, C // 32), np.uint8)
+    for i, s in enumerate(pipe.slices):
+        oracle.quant_mx_into(bf16_bits(s[:slice_rows]).reshape(slice_rows, HIDDEN), qb, sbuf, i * HIDDEN)
+    ok["quant_mx"] = same(pipe.mx_q[:slice_rows], qb) and same(pipe.mx_s[:slice_rows], sbuf)
+    ok["dequant_mx"] = same(pipe.mx_out[:slice_rows], oracle.dequant_mx(qb, sbuf))
+    return {"rows": rows, "slice_rows": slice_rows, "bitexact": all(ok.values()), "per_kernel": ok}
+
+
+def run_env(dev) -> dict:
+    """Where the numbers were taken: device, its UUID and SM count, driver, CUDA
+    runtime, torch, and the hash of the kernel sources."""
+    props = torch.cuda.get_device_properties(dev)
+    env = {"device": torch.cuda.get_device_name(dev), "uuid": str(getattr(props, "uuid", "")),
+           "sm_count": props.multi_processor_count, "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
+           "kernel_sources_sha": kernel_sources_sha(), "driver": None}
+    try:
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        buf = ctypes.create_string_buffer(96)
+        if nv.nvmlInit_v2() == 0 and nv.nvmlSystemGetDriverVersion(buf, 96) == 0:
+            env["driver"] = buf.value.decode()
+    except OSError:
+        pass
+    return env
+
+
 def cpu_inputs(rows: int, slice_rows: int):
     """Workload inputs for the CPU oracle leg: the first rows of the GPU-drawn buffers
     when a GPU exists (the very bits the GPU path consumes), else CPU draws."""
@@ -712,8 +767,8 @@ def run_profile_op(args):
                 codec.quant_mx_tiled(sl[i], q[:, c0:c0 + HIDDEN], tiled, g_total, c0 // 32)
             else:
                 codec.quant_mx(sl[i], q[:, c0:c0 + HIDDEN], s[:, c0 // 32:(c0 + HIDDEN) // 32])
-        codec.quant_mx_slices(sl, q, s)
         if op == "dequant_mx":
+            codec.quant_mx_slices(sl, q, s)  # the materialization's input
             del sl
             out = torch.empty((args.slice_rows, HIDDEN * N_SLICES), dtype=torch.bfloat16, device=dev)
             fn = lambda: codec.dequant_mx(q, s, out)
@@ -942,7 +997,9 @@ def run_bq(args, rank, world, local):
         ci = ([x[:r].cpu() for x in pipe.xs], [s[:sr].cpu() for s in pipe.slices])
         dt1, nb1 = oracle_sample(ci, r1, sr1, 1)
         dt, nb = oracle_sample(ci, r, sr, T)
+        parity = oracle_parity(pipe, min(64, args.rows), min(64, args.slice_rows))
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": T, "kind": "oracle",
+               "parity_sample": parity,
                "sample": f"one step of the same pipeline on the first {r} of {args.rows} rows of each INT8 buffer "
                          f"and the first {sr} of {args.slice_rows} rows of each MX slice, cut into {T} row ranges "
                          f"run by {T} host threads ({nb} algorithmic bytes, {dt:.2f} s wall)",
@@ -961,7 +1018,7 @@ def run_bq(args, rank, world, local):
         "step_samples_ms": [round(t, 4) for t in step_ms[:RAW_SAMPLES]],
         "roofline": roofline, "kernels": kernels, "next_rows": next_rows, "configs": configs, "clocks": clocks,
         "e2e": e2e, "gpu_launches": nl * args.steps, "cpu_baseline": cpu,
-        "device": torch.cuda.get_device_name(dev),
+        "device": torch.cuda.get_device_name(dev), "env": run_env(dev),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
