@@ -119,3 +119,9 @@ def test_mx_past_2_pow_31_elements():
     _same(bits(q[idx]), rq, "quant_mx codes")
     _same(bits(s[idx]), rs, "quant_mx E8M0")
     _same(bits(out[idx]), oracle.dequant_mx(rq, rs), "dequant_mx")
+    # the same matrix as two strided half-width slices quantized by one call: the bytes of
+    # the single call, every one of them (the destination holds more than 2^31 values)
+    del out
+    q2, s2 = codec.empty_mx(rows, cols)
+    codec.quant_mx_slices([x[:, :cols // 2], x[:, cols // 2:]], q2, s2)
+    assert torch.equal(q2, q) and torch.equal(s2, s)
