@@ -540,7 +540,8 @@ def oracle_parity(pipe, rows: int, slice_rows: int) -> dict:
 
 def run_env(dev) -> dict:
     """Where the numbers were taken: device, its UUID and SM count, driver, CUDA
-    runtime, torch, and the hash of the kernel sources."""
+    runtime, torch, the hash of the kernel sources, and the GPU's compute and
+    persistence modes (read-only NVML queries)."""
     props = torch.cuda.get_device_properties(dev)
     env = {"device": torch.cuda.get_device_name(dev), "uuid": str(getattr(props, "uuid", "")),
            "sm_count": props.multi_processor_count, "cuda_runtime": torch.version.cuda, "torch": torch.__version__,
@@ -551,7 +552,15 @@ def run_env(dev) -> dict:
         buf = ctypes.create_string_buffer(96)
         if nv.nvmlInit_v2() == 0 and nv.nvmlSystemGetDriverVersion(buf, 96) == 0:
             env["driver"] = buf.value.decode()
-    except OSError:
+        h, mode = ctypes.c_void_p(), ctypes.c_int()
+        uuid = env["uuid"] if env["uuid"].startswith("GPU-") else "GPU-" + env["uuid"]
+        if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0:
+            names = {0: "default", 2: "exclusive_process", 3: "prohibited"}
+            if nv.nvmlDeviceGetComputeMode(h, ctypes.byref(mode)) == 0:
+                env["compute_mode"] = names.get(mode.value, str(mode.value))
+            if nv.nvmlDeviceGetPersistenceMode(h, ctypes.byref(mode)) == 0:
+                env["persistence_mode"] = bool(mode.value)
+    except (OSError, AttributeError):
         pass
     return env
 
