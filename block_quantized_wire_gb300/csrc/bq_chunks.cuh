@@ -85,6 +85,116 @@ __device__ __forceinline__ void run_chunks(const Op &op, int64_t nblk, int chunk
     }
 }
 
+// A warp's shared-memory stage for one chunk's inputs copied lane by lane: NV4 slots
+// of 16 bytes and NU32 slots of 4 bytes per lane. Slot k of lane l sits at
+// (32k + l) * 16 (then (32k + l) * 4 after the 16-byte slots), so a warp reading one
+// slot reads 512 (or 128) contiguous bytes, free of bank conflicts.
+template <int NV4, int NU32>
+struct LaneSlots {
+    static constexpr uint32_t kBytes = NV4 * 512u + NU32 * 128u;
+    const unsigned char *p;  // the stage, generic address
+    uint32_t a;              // the stage, shared-window address
+    int lane;
+    __device__ __forceinline__ void copy_v4(int k, const void *src) const
+    {
+        lane_copy16(a + (32u * k + lane) * 16u, src);
+    }
+    __device__ __forceinline__ void copy_u32(int k, const void *src) const
+    {
+        lane_copy4(a + NV4 * 512u + (32u * k + lane) * 4u, src);
+    }
+    __device__ __forceinline__ uint4 v4(int k) const
+    {
+        return *reinterpret_cast<const uint4 *>(p + (32u * k + lane) * 16u);
+    }
+    __device__ __forceinline__ uint32_t u32(int k) const
+    {
+        return *reinterpret_cast<const uint32_t *>(p + NV4 * 512u + (32u * k + lane) * 4u);
+    }
+};
+
+// The wide accumulates' inputs for one full chunk c of exactly W sources, as per-lane
+// copies: each source's 16 payload bytes in both 512-value segments (slots 2i, 2i + 1)
+// and, in lanes 0..7, the scale word of the chunk's block `lane` (slot i). take fills
+// the accumulates' In {q[W][2], sc[W]} exactly as their global-memory load does.
+template <int W, class List>
+__device__ __forceinline__ void issue_wide_sources(const LaneSlots<2 * W, W> &sl, const List &src, int64_t c,
+                                                   int lane)
+{
+    const int64_t e0 = c * 1024 + lane * 16, b0 = c * 8;
+#pragma unroll
+    for (int i = 0; i < W; i++)
+#pragma unroll
+        for (int j = 0; j < 2; j++) sl.copy_v4(2 * i + j, src.q[i] + e0 + 512 * j);
+    if (lane < 8) {
+#pragma unroll
+        for (int i = 0; i < W; i++) sl.copy_u32(i, src.s[i] + b0 + lane);
+    }
+}
+
+template <int W, class In>
+__device__ __forceinline__ void take_wide_sources(In &in, const LaneSlots<2 * W, W> &sl, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < W; i++) {
+#pragma unroll
+        for (int j = 0; j < 2; j++) in.q[i][j] = sl.v4(2 * i + j);
+        in.sc[i] = lane < 8 ? sl.u32(i) : 0u;  // lanes 8..31 copied no scale word
+    }
+}
+
+// Grid-stride driver whose loads run STAGES - 1 chunks ahead through per-lane async
+// copies into the warp's STAGES stages (warp_smem, STAGES * Op::Slots::kBytes bytes):
+// before chunk c is computed, the copies of chunk c + (STAGES - 1) * stride are issued,
+// so the warp's next inputs are in flight while it computes and hold no registers.
+// Op additionally provides
+//   Slots                               a LaneSlots type
+//   issue(const Slots&, c)              the lane's copies of full chunk c
+//   take(In&, const Slots&)             fill In from the stage, as load<false> would
+// A stage is overwritten only STAGES - 1 chunks after it was read, and its reads fed
+// that chunk's results, which were stored before the new copies are issued. The
+// ragged last chunk, if any, takes the global-memory path.
+template <int STAGES, class Op>
+__device__ __forceinline__ void run_chunks_lane_async(const Op &op, int64_t nblk, int chunk_blocks,
+                                                      unsigned char *warp_smem)
+{
+    using Slots = typename Op::Slots;
+    const int lane = threadIdx.x & 31;
+    const uint32_t a0 = smem_u32(warp_smem);
+    const int64_t nfull = nblk / chunk_blocks;
+    const int64_t stride = warp_count();
+    int64_t c = warp_id();
+    if (c < nfull) {
+#pragma unroll
+        for (int k = 0; k < STAGES - 1; k++) {
+            if (c + k * stride < nfull)
+                op.issue(Slots{warp_smem + k * Slots::kBytes, a0 + k * Slots::kBytes, lane}, c + k * stride);
+            lane_copy_commit();  // empty groups keep the count of groups in flight fixed
+        }
+        int st = 0;
+        while (true) {
+            const int64_t ahead = c + (STAGES - 1) * stride;
+            const int fst = (st + STAGES - 1) % STAGES;
+            if (ahead < nfull)
+                op.issue(Slots{warp_smem + fst * Slots::kBytes, a0 + fst * Slots::kBytes, lane}, ahead);
+            lane_copy_commit();
+            lane_copy_wait<STAGES - 1>();  // chunk c's group has completed
+            typename Op::In in;
+            op.take(in, Slots{warp_smem + st * Slots::kBytes, a0 + st * Slots::kBytes, lane});
+            op.template compute<false>(in, c);
+            c += stride;
+            st = (st + 1) % STAGES;
+            if (c >= nfull) break;
+        }
+    }
+    lane_copy_wait<0>();
+    if (c == nfull && nblk % chunk_blocks) {
+        typename Op::In t;
+        op.template load<true>(t, c);
+        op.template compute<true>(t, c);
+    }
+}
+
 // Staged driver: each warp keeps the inputs of its next STAGES full chunks in flight
 // as bulk copies into its own slice of shared memory (issued by lane 0, completed on
 // one mbarrier per stage), reads a chunk's inputs from shared memory into the same

@@ -221,6 +221,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     return true;
 }
 
+// ---------------------------------------------------------------- per-lane async copies
+// Global -> shared copies issued by each lane for its own bytes (cp.async, 16 or 4
+// bytes, bypassing L1 for 16), grouped per thread with commit_group and completed with
+// wait_group. A lane reads back only bytes it copied itself, so wait_group alone makes
+// them visible to it: no barrier, no mbarrier, no cross-lane synchronization. The wait
+// is for this thread's own copies of valid addresses, which complete like loads.
+// Both addresses aligned to the copy size.
+__device__ __forceinline__ void lane_copy16(uint32_t dst, const void *src)
+{
+    if (!dbg_ok(src, 16, false)) return;  // the slot keeps stale bytes; counted in debug builds
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void lane_copy4(uint32_t dst, const void *src)
+{
+    if (!dbg_ok(src, 4, false)) return;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void lane_copy_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Returns once at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void lane_copy_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- global memory
 // Inputs are read once: non-coherent path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
