@@ -59,6 +59,7 @@ std::atomic<int> g_sms[kMaxDevices];
 struct OccEntry {
     const void *kernel;
     size_t smem;
+    int block;
     int device;
     int ctas_per_sm;
 };
@@ -67,7 +68,7 @@ int g_occ_n = 0;
 std::mutex g_occ_mu;
 }  // namespace
 
-cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem)
+cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem, int block)
 {
     int dev = 0;
     if (cudaError_t e = cudaGetDevice(&dev)) return e;
@@ -80,7 +81,8 @@ cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem)
     {
         std::lock_guard<std::mutex> lock(g_occ_mu);
         for (int i = 0; i < g_occ_n; i++)
-            if (g_occ[i].kernel == kernel && g_occ[i].smem == smem && g_occ[i].device == dev) occ = g_occ[i].ctas_per_sm;
+            if (g_occ[i].kernel == kernel && g_occ[i].smem == smem && g_occ[i].block == block && g_occ[i].device == dev)
+                occ = g_occ[i].ctas_per_sm;
     }
     if (occ == 0) {
         if (smem > 48 * 1024) {
@@ -88,12 +90,12 @@ cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem)
                                                      static_cast<int>(smem)))
                 return e;
         }
-        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem)) return e;
+        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, block, smem)) return e;
         if (occ < 1) occ = 1;
         std::lock_guard<std::mutex> lock(g_occ_mu);
-        if (g_occ_n < kMaxKernels) g_occ[g_occ_n++] = OccEntry{kernel, smem, dev, occ};
+        if (g_occ_n < kMaxKernels) g_occ[g_occ_n++] = OccEntry{kernel, smem, block, dev, occ};
     }
-    const int64_t warps_per_cta = kThreads / 32;
+    const int64_t warps_per_cta = block / 32;
     const int64_t need = (nchunk + warps_per_cta - 1) / warps_per_cta;
     const int64_t full = static_cast<int64_t>(sms) * occ;
     *grid = static_cast<int>(need < full ? (need > 0 ? need : 1) : full);

@@ -42,8 +42,18 @@
 namespace bqk {
 namespace {
 
-__device__ __forceinline__ int64_t warp_id() { return ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5; }
-__device__ __forceinline__ int64_t warp_count() { return ((int64_t)gridDim.x * kThreads) >> 5; }
+// Warp index in the grid and number of warps, for a kernel launched with kBlock threads
+// per CTA (kThreads unless the kernel and its launch both say otherwise).
+template <int kBlock = kThreads>
+__device__ __forceinline__ int64_t warp_id()
+{
+    return ((int64_t)blockIdx.x * kBlock + threadIdx.x) >> 5;
+}
+template <int kBlock = kThreads>
+__device__ __forceinline__ int64_t warp_count()
+{
+    return ((int64_t)gridDim.x * kBlock) >> 5;
+}
 
 // Grid-stride driver over warp chunks. With kPrefetch, the loads of a warp's next
 // chunk (c + number of warps) are issued before chunk c is computed (a register
@@ -51,13 +61,14 @@ __device__ __forceinline__ int64_t warp_count() { return ((int64_t)gridDim.x * k
 //   In                                 registers holding one chunk's inputs
 //   load<kTail>(In&, c) / compute<kTail>(const In&, c)
 // Full chunks use kTail = false (no bounds checks); the one partial chunk, if any,
-// is loaded and computed by the warp whose stride lands on it.
-template <bool kPrefetch, class Op>
+// is loaded and computed by the warp whose stride lands on it. kBlock: threads per CTA
+// of the launch.
+template <bool kPrefetch, int kBlock = kThreads, class Op>
 __device__ __forceinline__ void run_chunks(const Op &op, int64_t nblk, int chunk_blocks)
 {
     const int64_t nfull = nblk / chunk_blocks;
-    const int64_t stride = warp_count();
-    int64_t c = warp_id();
+    const int64_t stride = warp_count<kBlock>();
+    int64_t c = warp_id<kBlock>();
     if (!kPrefetch) {
         for (; c < nfull; c += stride) {
             typename Op::In cur;
@@ -153,8 +164,9 @@ __device__ __forceinline__ void take_wide_sources(In &in, const LaneSlots<2 * W,
 //   take(In&, const Slots&)             fill In from the stage, as load<false> would
 // A stage is overwritten only STAGES - 1 chunks after it was read, and its reads fed
 // that chunk's results, which were stored before the new copies are issued. The
-// ragged last chunk, if any, takes the global-memory path.
-template <int STAGES, class Op>
+// ragged last chunk, if any, takes the global-memory path. kBlock: threads per CTA of
+// the launch.
+template <int STAGES, int kBlock = kThreads, class Op>
 __device__ __forceinline__ void run_chunks_lane_async(const Op &op, int64_t nblk, int chunk_blocks,
                                                       unsigned char *warp_smem)
 {
@@ -162,8 +174,8 @@ __device__ __forceinline__ void run_chunks_lane_async(const Op &op, int64_t nblk
     const int lane = threadIdx.x & 31;
     const uint32_t a0 = smem_u32(warp_smem);
     const int64_t nfull = nblk / chunk_blocks;
-    const int64_t stride = warp_count();
-    int64_t c = warp_id();
+    const int64_t stride = warp_count<kBlock>();
+    int64_t c = warp_id<kBlock>();
     if (c < nfull) {
 #pragma unroll
         for (int k = 0; k < STAGES - 1; k++) {

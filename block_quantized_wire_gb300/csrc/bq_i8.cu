@@ -436,9 +436,15 @@ struct HopWideI8 {
 #ifndef BQ_HOP_MIN_CTAS
 #define BQ_HOP_MIN_CTAS 4
 #endif
+// Threads per CTA of the wide hop (registers per thread at the BQ_HOP_MIN_CTAS budget).
+// One CTA per SM, all warps of the same age: 287.8 against 291.4 us with 256 threads.
+#ifndef BQ_HOP_WIDE_THREADS
+#define BQ_HOP_WIDE_THREADS 1024
+#endif
+constexpr int kHopWideThreads = BQ_HOP_WIDE_THREADS;
 
 template <bool kOut, bool kV8>
-__global__ void __launch_bounds__(kThreads, BQ_HOP_MIN_CTAS)
+__global__ void __launch_bounds__(kHopWideThreads, BQ_HOP_MIN_CTAS * kThreads / kHopWideThreads)
 ring_hop_i8_wide_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_in,
                         const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s,
                         uint16_t *__restrict__ out)
@@ -451,7 +457,7 @@ ring_hop_i8_wide_kernel(const int8_t *__restrict__ q_in, const float *__restrict
     dbg_bf16(out, nblk, true);
     dbg_ready();
     const HopWideI8<kOut, kV8> op{q_in, s_in, x, q, s, out, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<false>(op, nblk, 8);
+    run_chunks<false, kHopWideThreads>(op, nblk, 8);
 }
 
 #ifndef BQ_ACCUM_WIDE
@@ -471,13 +477,18 @@ ring_hop_i8_wide_kernel(const int8_t *__restrict__ q_in, const float *__restrict
 #ifndef BQ_ACCUM_ASYNC
 #define BQ_ACCUM_ASYNC 1
 #endif
-#ifndef BQ_ACCUM_ASYNC_MIN_CTAS
-#define BQ_ACCUM_ASYNC_MIN_CTAS 2
+// Threads per CTA, one CTA per SM at 512: the warp schedulers favour a CTA's warps by
+// the CTA's age, so of two 256-thread CTAs on an SM the older finishes about 14% of the
+// launch earlier and the other runs alone until the end. With all of the SM's warps in
+// one CTA they keep pace: 379 against 385 us for the four-source launch.
+#ifndef BQ_ACCUM_ASYNC_THREADS
+#define BQ_ACCUM_ASYNC_THREADS 512
 #endif
+constexpr int kAccumAsyncThreads = BQ_ACCUM_ASYNC_THREADS;
 constexpr int kAccumAsyncStages = 2;
 
 template <int W>
-__global__ void __launch_bounds__(kThreads, BQ_ACCUM_ASYNC_MIN_CTAS)
+__global__ void __launch_bounds__(kAccumAsyncThreads, kAccumAsyncThreads >= 512 ? 1 : 512 / kAccumAsyncThreads)
 accum_i8_async_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
                       float *__restrict__ s)
 {
@@ -489,8 +500,8 @@ accum_i8_async_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t 
     dbg_ready();
     using Op = AccumWideI8<W, false, false, false>;
     const Op op{src, nsrc, q, s, nullptr, nblk, (int)(threadIdx.x & 31)};
-    run_chunks_lane_async<kAccumAsyncStages>(op, nblk, 8,
-                                             stages + (threadIdx.x >> 5) * kAccumAsyncStages * Op::Slots::kBytes);
+    run_chunks_lane_async<kAccumAsyncStages, kAccumAsyncThreads>(
+        op, nblk, 8, stages + (threadIdx.x >> 5) * kAccumAsyncStages * Op::Slots::kBytes);
 }
 
 template <int W, bool kOut, bool kMore, bool kV8>
@@ -508,8 +519,17 @@ accum_i8_wide_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t n
     run_chunks<false>(op, nblk, 8);
 }
 
+// Threads per CTA of the wide quantize; its registers per thread stay at the 4-CTA
+// budget (64) whatever the CTA size. One CTA per SM (1024 threads) keeps all of an SM's
+// warps at the same age for the warp schedulers: 219.2 against 222.9 us per 469.8M-value
+// launch with 256-thread CTAs (221.3 with 512).
+#ifndef BQ_QUANT_WIDE_THREADS
+#define BQ_QUANT_WIDE_THREADS 1024
+#endif
+constexpr int kQuantWideThreads = BQ_QUANT_WIDE_THREADS;
+
 template <bool kV8>
-__global__ void __launch_bounds__(kThreads, BQ_QUANT_MIN_CTAS)
+__global__ void __launch_bounds__(kQuantWideThreads, BQ_QUANT_MIN_CTAS * kThreads / kQuantWideThreads)
 quant_i8_wide_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
@@ -518,7 +538,7 @@ quant_i8_wide_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__res
     dbg_wire(q, s, nblk, true);
     dbg_ready();
     const QuantWideI8<kV8> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<false>(op, nblk, 8);
+    run_chunks<false, kQuantWideThreads>(op, nblk, 8);
 }
 
 // ---------------------------------------------------------------- ring hop
@@ -621,10 +641,11 @@ cudaError_t launch_accum_wide(const SourceList &src, int nsrc, int64_t nblk, int
         if (BQ_ACCUM_ASYNC) {
             auto kernel = accum_i8_async_kernel<W>;
             const size_t smem =
-                (kThreads / 32) * kAccumAsyncStages * AccumWideI8<W, false, false, false>::Slots::kBytes;
+                (kAccumAsyncThreads / 32) * kAccumAsyncStages * AccumWideI8<W, false, false, false>::Slots::kBytes;
             int grid = 0;
-            if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, smem)) return e;
-            return launch_kernel_smem(kernel, grid, smem, st, src, nsrc, nblk, q, s);
+            if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, smem, kAccumAsyncThreads))
+                return e;
+            return launch_kernel_block(kernel, grid, kAccumAsyncThreads, smem, st, src, nsrc, nblk, q, s);
         }
     }
     auto kernel = accum_i8_wide_kernel<W, kOut, kMore, false>;
@@ -671,8 +692,9 @@ cudaError_t launch_quant_i8(const uint16_t *x, int64_t nblk, int8_t *q, float *s
 {
     if (BQ_QUANT_WIDE) {
         auto kernel = BQ_WIDE_V8 && aligned32(x) ? quant_i8_wide_kernel<true> : quant_i8_wide_kernel<false>;
-        BQK_GRID(kernel, chunks(nblk, 4));
-        return launch_kernel(kernel, grid, st, x, nblk, q, s);
+        int grid = 0;
+        if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, 0, kQuantWideThreads)) return e;
+        return launch_kernel_block(kernel, grid, kQuantWideThreads, 0, st, x, nblk, q, s);
     }
     return launch_quant_stages<kStagesQuant>(x, nblk, q, s, st);
 }
@@ -786,8 +808,9 @@ cudaError_t launch_ring_hop_i8(const int8_t *q_in, const float *s_in, const uint
         const bool v8 = BQ_WIDE_V8 && aligned32(x) && (!out || aligned32(out));
         auto kernel = out ? (v8 ? ring_hop_i8_wide_kernel<true, true> : ring_hop_i8_wide_kernel<true, false>)
                           : (v8 ? ring_hop_i8_wide_kernel<false, true> : ring_hop_i8_wide_kernel<false, false>);
-        BQK_GRID(kernel, chunks(nblk, 4));
-        return launch_kernel(kernel, grid, st, q_in, s_in, x, nblk, q, s, out);
+        int grid = 0;
+        if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, 0, kHopWideThreads)) return e;
+        return launch_kernel_block(kernel, grid, kHopWideThreads, 0, st, q_in, s_in, x, nblk, q, s, out);
     }
     if (out) return launch_hop_stages<kStagesHop, true>(q_in, s_in, x, nblk, q, s, out, st);
     return launch_hop_stages<kStagesHop, false>(q_in, s_in, x, nblk, q, s, nullptr, st);

@@ -80,11 +80,12 @@ cudaError_t launch_reduce_quant_e4m3(const Bf16List &src, int W, int64_t nblk, u
 #endif
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel_smem(void (*kernel)(KArgs...), int grid, size_t smem, cudaStream_t st, Args... args)
+cudaError_t launch_kernel_block(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t st,
+                                Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -96,17 +97,23 @@ cudaError_t launch_kernel_smem(void (*kernel)(KArgs...), int grid, size_t smem, 
 }
 
 template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_smem(void (*kernel)(KArgs...), int grid, size_t smem, cudaStream_t st, Args... args)
+{
+    return launch_kernel_block(kernel, grid, kThreads, smem, st, args...);
+}
+
+template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, cudaStream_t st, Args... args)
 {
     return launch_kernel_smem(kernel, grid, 0, st, args...);
 }
 
 // Grid size for a grid-stride kernel over `nchunk` warp chunks with `smem` bytes of
-// dynamic shared memory per CTA: enough CTAs to fill every SM of the current device at
-// the kernel's occupancy, and no more CTAs than there are chunks. The first call for a
-// kernel also raises its dynamic shared memory limit to `smem`. Returns the error of
-// the device queries, if any.
-cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem = 0);
+// dynamic shared memory per CTA of `block` threads: enough CTAs to fill every SM of the
+// current device at the kernel's occupancy, and no more CTAs than there are chunks. The
+// first call for a kernel also raises its dynamic shared memory limit to `smem`. Returns
+// the error of the device queries, if any.
+cudaError_t grid_for(const void *kernel, int64_t nchunk, int *grid, size_t smem = 0, int block = kThreads);
 
 // Each kernel translation unit's counters {wait timeouts, unlanded copies, debug index errors} (see
 // g_wait_timeouts in bq_device.cuh): totals since the library was loaded, never reset.

@@ -400,13 +400,16 @@ accum_mx_wide_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t
 #ifndef BQ_ACCUM_MX_ASYNC
 #define BQ_ACCUM_MX_ASYNC 1
 #endif
-#ifndef BQ_ACCUM_MX_ASYNC_MIN_CTAS
-#define BQ_ACCUM_MX_ASYNC_MIN_CTAS 2
+// Threads per CTA (one CTA per SM at 512, so that all of an SM's warps have the same
+// age for the warp schedulers): 363 against 368 us for the four-source launch.
+#ifndef BQ_ACCUM_MX_ASYNC_THREADS
+#define BQ_ACCUM_MX_ASYNC_THREADS 512
 #endif
+constexpr int kAccumMxAsyncThreads = BQ_ACCUM_MX_ASYNC_THREADS;
 constexpr int kAccumMxAsyncStages = 2;
 
 template <int W>
-__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MX_ASYNC_MIN_CTAS)
+__global__ void __launch_bounds__(kAccumMxAsyncThreads, kAccumMxAsyncThreads >= 512 ? 1 : 512 / kAccumMxAsyncThreads)
 accum_mx_async_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t nblk, uint8_t *__restrict__ q,
                       uint32_t *__restrict__ s)
 {
@@ -418,8 +421,8 @@ accum_mx_async_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_
     dbg_ready();
     using Op = AccumWideMx<W, false, false, false>;
     const Op op{src, nsrc, q, s, nullptr, nblk, (int)(threadIdx.x & 31)};
-    run_chunks_lane_async<kAccumMxAsyncStages>(op, nblk, 8,
-                                               stages + (threadIdx.x >> 5) * kAccumMxAsyncStages * Op::Slots::kBytes);
+    run_chunks_lane_async<kAccumMxAsyncStages, kAccumMxAsyncThreads>(
+        op, nblk, 8, stages + (threadIdx.x >> 5) * kAccumMxAsyncStages * Op::Slots::kBytes);
 }
 
 template <bool kOut, bool kV8>
@@ -466,10 +469,11 @@ cudaError_t launch_accum_mx_wide(const MxSourceList &src, int nsrc, int64_t nblk
         if (BQ_ACCUM_MX_ASYNC && !o) {
             auto kernel = accum_mx_async_kernel<W>;
             const size_t smem =
-                (kThreads / 32) * kAccumMxAsyncStages * AccumWideMx<W, false, false, false>::Slots::kBytes;
+                (kAccumMxAsyncThreads / 32) * kAccumMxAsyncStages * AccumWideMx<W, false, false, false>::Slots::kBytes;
             int grid = 0;
-            if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, smem)) return e;
-            return launch_kernel_smem(kernel, grid, smem, st, src, nsrc, nblk, q, s);
+            if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, smem, kAccumMxAsyncThreads))
+                return e;
+            return launch_kernel_block(kernel, grid, kAccumMxAsyncThreads, smem, st, src, nsrc, nblk, q, s);
         }
     }
     auto kernel = o ? (v8 ? accum_mx_wide_kernel<W, true, kMore, true> : accum_mx_wide_kernel<W, true, kMore, false>)
