@@ -65,9 +65,21 @@ struct E4m3Codec {
 #ifndef BQ_QUANT_E4M3_MIN_CTAS
 #define BQ_QUANT_E4M3_MIN_CTAS 4
 #endif
+// Threads per CTA of the E4M3 quantize and materialize (registers per thread at the
+// 4-CTA budget of 256-thread CTAs whatever the size). Per 469.8M-value launch on GB300:
+// quantize 231.6 us in one 1024-thread CTA per SM against 241.9 us in 256-thread CTAs;
+// the materialize 247.7 against 241.7 us, so it keeps 256.
+#ifndef BQ_QUANT_E4M3_THREADS
+#define BQ_QUANT_E4M3_THREADS 1024
+#endif
+#ifndef BQ_DEQUANT_E4M3_THREADS
+#define BQ_DEQUANT_E4M3_THREADS 256
+#endif
+constexpr int kQuantE4m3Threads = BQ_QUANT_E4M3_THREADS;
+constexpr int kDequantE4m3Threads = BQ_DEQUANT_E4M3_THREADS;
 
 template <int SEGS>
-__global__ void __launch_bounds__(kThreads, BQ_QUANT_E4M3_MIN_CTAS)
+__global__ void __launch_bounds__(kQuantE4m3Threads, BQ_QUANT_E4M3_MIN_CTAS * kThreads / kQuantE4m3Threads)
 quant_e4m3_kernel(const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restrict__ q, float *__restrict__ s)
 {
     pdl_begin();
@@ -76,11 +88,11 @@ quant_e4m3_kernel(const uint16_t *__restrict__ x, int64_t nblk, uint8_t *__restr
     dbg_wire(q, s, nblk, true);
     dbg_ready();
     const QuantOp<E4m3Codec, SEGS, true> op{x, q, s, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<false>(op, nblk, 2 * SEGS);
+    run_chunks<false, kQuantE4m3Threads>(op, nblk, 2 * SEGS);
 }
 
 template <int SEGS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kDequantE4m3Threads, 4 * kThreads / kDequantE4m3Threads)
 dequant_e4m3_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk,
                     uint16_t *__restrict__ out)
 {
@@ -90,7 +102,7 @@ dequant_e4m3_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s, 
     dbg_bf16(out, nblk, true);
     dbg_ready();
     const DequantOp<E4m3Codec, SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<true>(op, nblk, 2 * SEGS);
+    run_chunks<true, kDequantE4m3Threads>(op, nblk, 2 * SEGS);
 }
 
 template <int SEGS, int W, bool kOut>
@@ -106,6 +118,25 @@ reduce_quant_e4m3_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t
     dbg_ready();
     const ReduceQuantOp<E4m3Codec, SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
+}
+
+#ifndef BQ_SEGS_REDUCE_E4M3_ASYNC
+#define BQ_SEGS_REDUCE_E4M3_ASYNC 2
+#endif
+
+template <int W, bool kOut>
+__global__ void __launch_bounds__(kReduceAsyncThreads, kReduceAsyncMinCtas)
+reduce_quant_e4m3_async_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t nblk, uint8_t *__restrict__ q,
+                               float *__restrict__ s, uint16_t *__restrict__ out)
+{
+    extern __shared__ __align__(16) unsigned char stages[];
+    pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
+    reduce_quant_async_body<E4m3Codec, BQ_SEGS_REDUCE_E4M3_ASYNC, W, kOut>(src, nsrc, nblk, q, s, out, stages);
 }
 
 // E4M3 quantize, 469.8M values on GB300 (graph-timed): 264 us with 4 segments per chunk
@@ -128,6 +159,9 @@ template <int W, bool kOut>
 cudaError_t launch_reduce_w(const Bf16List &src, int nsrc, int64_t nblk, uint8_t *q, float *s, uint16_t *out,
                             cudaStream_t st)
 {
+    if (BQ_REDUCE_ASYNC && nsrc == W)
+        return launch_reduce_async<E4m3Codec, BQ_SEGS_REDUCE_E4M3_ASYNC, W, kOut>(
+            reduce_quant_e4m3_async_kernel<W, kOut>, nblk, st, src, nsrc, nblk, q, s, out);
     auto kernel = reduce_quant_e4m3_kernel<kSegsReduce, W, kOut>;
     BQK_GRID(kernel, chunks(nblk, kSegsReduce));
     return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
@@ -137,14 +171,19 @@ cudaError_t launch_reduce_w(const Bf16List &src, int nsrc, int64_t nblk, uint8_t
 
 cudaError_t launch_quant_e4m3(const uint16_t *x, int64_t nblk, uint8_t *q, float *s, cudaStream_t st)
 {
-    BQK_GRID(quant_e4m3_kernel<kSegsQuant>, chunks(nblk, kSegsQuant));
-    return launch_kernel(quant_e4m3_kernel<kSegsQuant>, grid, st, x, nblk, q, s);
+    auto kernel = quant_e4m3_kernel<kSegsQuant>;
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, kSegsQuant), &grid, 0, kQuantE4m3Threads)) return e;
+    return launch_kernel_block(kernel, grid, kQuantE4m3Threads, 0, st, x, nblk, q, s);
 }
 
 cudaError_t launch_dequant_e4m3(const uint8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
 {
-    BQK_GRID(dequant_e4m3_kernel<kSegsDequant>, chunks(nblk, kSegsDequant));
-    return launch_kernel(dequant_e4m3_kernel<kSegsDequant>, grid, st, q, s, nblk, out);
+    auto kernel = dequant_e4m3_kernel<kSegsDequant>;
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, kSegsDequant), &grid, 0, kDequantE4m3Threads))
+        return e;
+    return launch_kernel_block(kernel, grid, kDequantE4m3Threads, 0, st, q, s, nblk, out);
 }
 
 // One source width per common case (1..4 at once); more sources in groups of four.

@@ -580,6 +580,10 @@ ring_hop_i8_kernel(const int8_t *__restrict__ q_in, const float *__restrict__ s_
 }
 
 // ---------------------------------------------------------------- reduce + quantize
+#ifndef BQ_SEGS_REDUCE_I8_ASYNC
+#define BQ_SEGS_REDUCE_I8_ASYNC 2
+#endif
+
 template <int SEGS, int W, bool kOut>
 __global__ void __launch_bounds__(kThreads)
 reduce_quant_i8_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
@@ -593,6 +597,21 @@ reduce_quant_i8_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t n
     dbg_ready();
     const ReduceQuantOp<I8Codec, SEGS, W, kOut> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
     run_chunks<false>(op, nblk, 2 * SEGS);
+}
+
+template <int W, bool kOut>
+__global__ void __launch_bounds__(kReduceAsyncThreads, kReduceAsyncMinCtas)
+reduce_quant_i8_async_kernel(const __grid_constant__ Bf16List src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
+                             float *__restrict__ s, uint16_t *__restrict__ out)
+{
+    extern __shared__ __align__(16) unsigned char stages[];
+    pdl_begin();
+    dbg_begin();
+    dbg_sources(src, nsrc, nblk);
+    dbg_wire(q, s, nblk, true);
+    dbg_bf16(out, nblk, true);
+    dbg_ready();
+    reduce_quant_async_body<I8Codec, BQ_SEGS_REDUCE_I8_ASYNC, W, kOut>(src, nsrc, nblk, q, s, out, stages);
 }
 
 // Segments per warp chunk for each kernel (tuned on GB300; overridable at build time).
@@ -821,6 +840,9 @@ template <int W, bool kOut>
 cudaError_t launch_reduce_i8_w(const Bf16List &src, int nsrc, int64_t nblk, int8_t *q, float *s, uint16_t *out,
                                cudaStream_t st)
 {
+    if (BQ_REDUCE_ASYNC && nsrc == W)
+        return launch_reduce_async<I8Codec, BQ_SEGS_REDUCE_I8_ASYNC, W, kOut>(
+            reduce_quant_i8_async_kernel<W, kOut>, nblk, st, src, nsrc, nblk, q, s, out);
     auto kernel = reduce_quant_i8_kernel<kSegsReduce, W, kOut>;
     BQK_GRID(kernel, chunks(nblk, kSegsReduce));
     return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);

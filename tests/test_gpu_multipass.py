@@ -5,9 +5,10 @@ exercised beyond their first pass. Bit-exact against the oracle; outputs framed 
 guard bands.
 
 Operations: "feat(pcie_dma): add block-INT8 wire modes for AG, ring, and A2A",
-Implementation (quantize, materialize, multi-source accumulate, ring hop), and
-"feat(pcie_dma): add INT8 and MXFP8 wire modes", Summary (the same topologies on MX
-wires)."""
+Implementation (quantize, materialize, multi-source accumulate, ring hop) and Summary
+(the i8 all-gather mode, whose BF16 reduce is fused with quantization here, and the
+legacy E4M3 codec it is compared against), and "feat(pcie_dma): add INT8 and MXFP8 wire
+modes", Summary (the same topologies on MX wires)."""
 import numpy as np
 import pytest
 import torch
@@ -120,3 +121,39 @@ def test_mx_accumulate_multipass(W):
     same(gq.view(torch.uint8), qa, "MX accumulated codes")
     same(gs.view(torch.uint8), sa, "MX accumulated scales")
     assert gq.bands_intact() and gs.bands_intact()
+
+
+@pytest.mark.parametrize("owner", [False, True])
+@pytest.mark.parametrize("W", [1, 2, 4, 5])
+@pytest.mark.parametrize("codec_name", ["i8", "e4m3"])
+def test_reduce_quant_multipass(i8_sources, codec_name, W, owner):
+    # W <= 4: the per-lane async copy kernel of exactly W sources; 5: groups of four
+    nblk, xs, _ = i8_sources
+    n = nblk * 128
+    xd = [from_bits_bf16(x) for x in xs[:W]]
+    gq, gs, go = Guarded(n), Guarded(4 * nblk), Guarded(2 * n)
+    qt = torch.int8 if codec_name == "i8" else torch.uint8
+    run = codec.reduce_quant_i8 if codec_name == "i8" else codec.reduce_quant_e4m3
+    run(xd, gq.view(qt), gs.view(torch.float32), go.view(torch.bfloat16) if owner else None)
+    ref = oracle.reduce_quant_i8 if codec_name == "i8" else oracle.reduce_quant_e4m3
+    qr, sr, orr = ref(xs[:W], materialize=owner)
+    same(gq.view(qt), qr, f"{codec_name} reduced payload")
+    same(gs.view(torch.float32), sr, f"{codec_name} reduced scales")
+    if owner:
+        same(go.view(torch.bfloat16), orr, f"{codec_name} reduced materialized")
+    else:
+        assert (go.raw == Guarded.SENTINEL).all().item()
+    assert gq.bands_intact() and gs.bands_intact() and go.bands_intact()
+
+
+def test_e4m3_quant_dequant_multipass(i8_sources):
+    nblk, xs, _ = i8_sources
+    n = nblk * 128
+    gq, gs, go = Guarded(n), Guarded(4 * nblk), Guarded(2 * n)
+    codec.quant_e4m3(from_bits_bf16(xs[2]), gq.view(torch.uint8), gs.view(torch.float32))
+    qr, sr = oracle.quant_e4m3(xs[2])
+    same(gq.view(torch.uint8), qr, "E4M3 codes")
+    same(gs.view(torch.float32), sr, "E4M3 scales")
+    codec.dequant_e4m3(gq.view(torch.uint8), gs.view(torch.float32), go.view(torch.bfloat16))
+    same(go.view(torch.bfloat16), oracle.dequant_e4m3(qr, sr), "E4M3 materialized")
+    assert gq.bands_intact() and gs.bands_intact() and go.bands_intact()
