@@ -504,8 +504,18 @@ accum_i8_async_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t 
         op, nblk, 8, stages + (threadIdx.x >> 5) * kAccumAsyncStages * Op::Slots::kBytes);
 }
 
+// Threads per CTA of the wide accumulate with direct loads (the owner-output form and
+// launches of more than four sources); registers per thread at the BQ_ACCUM_MIN_CTAS
+// budget of 256-thread CTAs whatever the size. One 768-thread CTA per SM measured within
+// noise of three 256-thread CTAs for the four-source owner-output launch (576.2 against
+// 579.9 us, medians; the minima the other way round).
+#ifndef BQ_ACCUM_WIDE_THREADS
+#define BQ_ACCUM_WIDE_THREADS 256
+#endif
+constexpr int kAccumWideThreads = BQ_ACCUM_WIDE_THREADS;
+
 template <int W, bool kOut, bool kMore, bool kV8>
-__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MIN_CTAS)
+__global__ void __launch_bounds__(kAccumWideThreads, BQ_ACCUM_MIN_CTAS * kThreads / kAccumWideThreads)
 accum_i8_wide_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t nblk, int8_t *__restrict__ q,
                      float *__restrict__ s, uint16_t *__restrict__ out)
 {
@@ -516,7 +526,7 @@ accum_i8_wide_kernel(const __grid_constant__ SourceList src, int nsrc, int64_t n
     dbg_bf16(out, nblk, true);
     dbg_ready();
     const AccumWideI8<W, kOut, kMore, kV8> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<false>(op, nblk, 8);
+    run_chunks<false, kAccumWideThreads>(op, nblk, 8);
 }
 
 // Threads per CTA of the wide quantize; its registers per thread stay at the 4-CTA
@@ -670,8 +680,9 @@ cudaError_t launch_accum_wide(const SourceList &src, int nsrc, int64_t nblk, int
     auto kernel = accum_i8_wide_kernel<W, kOut, kMore, false>;
     if constexpr (kOut)
         if (BQ_WIDE_V8 && aligned32(out)) kernel = accum_i8_wide_kernel<W, kOut, kMore, true>;
-    BQK_GRID(kernel, chunks(nblk, 4));
-    return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, 0, kAccumWideThreads)) return e;
+    return launch_kernel_block(kernel, grid, kAccumWideThreads, 0, st, src, nsrc, nblk, q, s, out);
 }
 
 template <int W, bool kOut, bool kMore>

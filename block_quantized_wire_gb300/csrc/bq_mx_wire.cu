@@ -378,8 +378,16 @@ ring_hop_mx_staged_kernel(const uint8_t *__restrict__ q_in, const uint32_t *__re
     run_staged<STAGES>(op, nblk, 2 * SEGS, smem + (threadIdx.x >> 5) * staged_warp_bytes<HopMx<SEGS, kOut>, STAGES>());
 }
 
+// Threads per CTA of the wide MX accumulate with direct loads (the owner-output form and
+// launches of more than four sources); registers at the 256-thread budget. One 768-thread
+// CTA per SM measured within noise of three 256-thread CTAs (576.3 against 582.2 us).
+#ifndef BQ_ACCUM_MX_WIDE_THREADS
+#define BQ_ACCUM_MX_WIDE_THREADS 256
+#endif
+constexpr int kAccumMxWideThreads = BQ_ACCUM_MX_WIDE_THREADS;
+
 template <int W, bool kOut, bool kMore, bool kV8>
-__global__ void __launch_bounds__(kThreads, BQ_ACCUM_MX_MIN_CTAS)
+__global__ void __launch_bounds__(kAccumMxWideThreads, BQ_ACCUM_MX_MIN_CTAS * kThreads / kAccumMxWideThreads)
 accum_mx_wide_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t nblk, uint8_t *__restrict__ q,
                      uint32_t *__restrict__ s, uint16_t *__restrict__ out)
 {
@@ -390,7 +398,7 @@ accum_mx_wide_kernel(const __grid_constant__ MxSourceList src, int nsrc, int64_t
     dbg_bf16(out, nblk, true);
     dbg_ready();
     const AccumWideMx<W, kOut, kMore, kV8> op{src, nsrc, q, s, out, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<false>(op, nblk, 8);
+    run_chunks<false, kAccumMxWideThreads>(op, nblk, 8);
 }
 
 // The accumulate of exactly W sources without the owner output, with each warp's next
@@ -478,8 +486,9 @@ cudaError_t launch_accum_mx_wide(const MxSourceList &src, int nsrc, int64_t nblk
     }
     auto kernel = o ? (v8 ? accum_mx_wide_kernel<W, true, kMore, true> : accum_mx_wide_kernel<W, true, kMore, false>)
                     : accum_mx_wide_kernel<W, false, kMore, false>;
-    BQK_GRID(kernel, chunks(nblk, 4));
-    return launch_kernel(kernel, grid, st, src, nsrc, nblk, q, s, out);
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)kernel, chunks(nblk, 4), &grid, 0, kAccumMxWideThreads)) return e;
+    return launch_kernel_block(kernel, grid, kAccumMxWideThreads, 0, st, src, nsrc, nblk, q, s, out);
 }
 
 template <int W, bool kOut, bool kMore>
