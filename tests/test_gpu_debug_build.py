@@ -5,19 +5,21 @@ the byte ranges of the buffers its arguments describe (inputs read-only, outputs
 writable). Every global load, store and bulk copy is then checked against them; an access
 outside them is not performed and is counted. This module reruns parity tests through
 that build, covering every kernel family, ragged sizes, every source count, strided and
-staged MX, and 4-byte-aligned scales. The results must stay bit-exact and the count of
+staged MX, 4-byte-aligned scales, and sizes where every warp walks several chunks. The results must stay bit-exact and the count of
 declined accesses must stay 0. A self-test shows that an access outside the listed
 ranges is declined and counted, without it touching memory.
 """
 import pytest
 import torch
 
+import oracle
 from block_quantized_wire_gb300 import _lib, build, codec
 from block_quantized_wire_gb300._lib import BQError
 from tests import test_gpu_i8 as t8
 from tests import test_gpu_mx as tx
 from tests import test_gpu_mx_wire as tw
 from tests import test_gpu_next_rows as tn
+from tests import test_gpu_multipass as tm
 from tests import test_gpu_properties as tp
 
 pytestmark = pytest.mark.gpu
@@ -110,4 +112,23 @@ def test_allgather_and_e4m3_kernels_stay_in_bounds(dbg):
         tn.test_e4m3_input_aligned_to_16_but_not_32_bytes()
         tn.test_e4m3_scales_across_the_exact_division_cutoff()
         tp.test_fused_owner_output_equals_separate_materialization()
+        assert _no_declined_access()
+
+
+def test_multipass_kernels_stay_in_bounds(dbg):
+    # every warp several chunks deep: the async copy stages refilled, the grid-stride
+    # loops of the one-CTA-per-SM launches past their first pass, then a ragged tail
+    nblk = tm.multipass_nblk()
+    xs = [tm.source_bits(900 + i, nblk) for i in range(4)]
+    sources = (nblk, xs, [oracle.quant_i8(x) for x in xs])
+    with _lib.use_library(dbg):
+        codec.take_index_errors()
+        tm.test_quant_dequant_multipass(sources)
+        tm.test_ring_hop_multipass(sources, True)
+        for W in (1, 4):
+            tm.test_accumulate_multipass(sources, W, False)
+        for name in ("i8", "e4m3"):
+            tm.test_reduce_quant_multipass(sources, name, 4, False)
+        tm.test_e4m3_quant_dequant_multipass(sources)
+        tm.test_mx_accumulate_multipass(4)
         assert _no_declined_access()
