@@ -162,7 +162,7 @@ __device__ __forceinline__ void quant_mx_compute_any(const uint4 (&raw)[kSegs], 
 
 // Grid-stride walk over chunks with the chunk's (row, column block) advanced
 // incrementally: one division per warp at the start instead of one per chunk.
-template <int CB>
+template <int CB, int kBlock = kThreads>
 struct ChunkWalkT {
     int64_t c, stride, b0, step;
     ChunkPos pos;
@@ -171,8 +171,8 @@ struct ChunkWalkT {
     __device__ __forceinline__ ChunkWalkT(int64_t bpr_, int64_t cta, int64_t ncta)
     {
         bpr = bpr_;
-        stride = (ncta * kThreads) >> 5;
-        c = (cta * kThreads + threadIdx.x) >> 5;
+        stride = (ncta * kBlock) >> 5;
+        c = (cta * kBlock + threadIdx.x) >> 5;
         b0 = c * CB;
         pos.row0 = b0 / bpr;
         pos.cb0 = b0 - pos.row0 * bpr;
@@ -192,7 +192,6 @@ struct ChunkWalkT {
         }
     }
 };
-using ChunkWalk = ChunkWalkT<kChunkBlocks>;
 
 // 4 resident CTAs per SM (64 registers, no spills): 16.4 us per 4096x7168 slice on
 // GB300 against 16.8 us at 3 CTAs per SM. Issuing the next chunk's loads before
@@ -204,14 +203,14 @@ using ChunkWalk = ChunkWalkT<kChunkBlocks>;
 // Quantize one [rows, bpr * 128] matrix with ncta CTAs, this one being number cta.
 // kF16: the input is FP16 instead of BF16. kTiled: scales go to the tiled GEMM layout
 // (see scale_offset), c0 the slice's first tile column.
-template <bool kF16, bool kTiled>
+template <bool kF16, bool kTiled, int kBlock = kThreads>
 __device__ __forceinline__ void quant_mx_matrix(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk,
                                                 uint8_t *__restrict__ q, int64_t ld_q, uint8_t *__restrict__ s,
                                                 int64_t ld_s, int64_t c0, int64_t cta, int64_t ncta)
 {
     const int lane = threadIdx.x & 31;
     const int64_t nfull = nblk / kChunkBlocks;
-    ChunkWalk w(bpr, cta, ncta);
+    ChunkWalkT<kChunkBlocks, kBlock> w(bpr, cta, ncta);
     for (; w.c < nfull; w.next()) {
         uint4 raw[kSegs];
         quant_mx_load_any<false>(x, ld_x, bpr, nblk, w.b0, w.pos, lane, raw);
@@ -224,8 +223,18 @@ __device__ __forceinline__ void quant_mx_matrix(const uint16_t *__restrict__ x, 
     }
 }
 
+// Threads per CTA of the MX quantize (registers per thread at the BQ_QUANT_MX_MIN_CTAS
+// budget of 256-thread CTAs whatever the size). For the 89 MB slices of the prefill step
+// 256, 512 and 1024 threads measured the same inside the step: 20.5 us per launch with an
+// event after every launch, and the same step time, so the launch's fixed cost is not
+// the distribution of its CTAs.
+#ifndef BQ_QUANT_MX_THREADS
+#define BQ_QUANT_MX_THREADS 256
+#endif
+constexpr int kQuantMxThreads = BQ_QUANT_MX_THREADS;
+
 template <bool kF16, bool kTiled>
-__global__ void __launch_bounds__(kThreads, BQ_QUANT_MX_MIN_CTAS)
+__global__ void __launch_bounds__(kQuantMxThreads, BQ_QUANT_MX_MIN_CTAS * kThreads / kQuantMxThreads)
 quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64_t nblk, uint8_t *__restrict__ q,
                 int64_t ld_q, uint8_t *__restrict__ s, int64_t ld_s, int64_t c0)
 {
@@ -241,7 +250,7 @@ quant_mx_kernel(const uint16_t *__restrict__ x, int64_t ld_x, int64_t bpr, int64
             dbg_allow_2d(s, rows, 4 * bpr, ld_s, true);
     }
     dbg_ready();
-    quant_mx_matrix<kF16, kTiled>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, blockIdx.x, gridDim.x);
+    quant_mx_matrix<kF16, kTiled, kQuantMxThreads>(x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0, blockIdx.x, gridDim.x);
 }
 
 // Several staged slices in one launch (bq_quant_mx_slices): the CTAs are split between
@@ -358,8 +367,11 @@ cudaError_t launch_quant_mx_any(const uint16_t *x, int64_t ld_x, int64_t rows, i
 {
     const int64_t bpr = cols / 128, nblk = rows * bpr;
     auto kernel = quant_mx_kernel<kF16, kTiled>;
-    BQK_GRID(kernel, (nblk + kChunkBlocks - 1) / kChunkBlocks);
-    return launch_kernel(kernel, grid, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0);
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)kernel, (nblk + kChunkBlocks - 1) / kChunkBlocks, &grid, 0,
+                                 kQuantMxThreads))
+        return e;
+    return launch_kernel_block(kernel, grid, kQuantMxThreads, 0, st, x, ld_x, bpr, nblk, q, ld_q, s, ld_s, c0);
 }
 }  // namespace
 
