@@ -54,7 +54,7 @@ namespace bqk {
 
 namespace {
 constexpr int kMaxDevices = 64;
-constexpr int kMaxKernels = 1024;  // (kernel, dynamic smem, device) entries
+constexpr int kMaxKernels = 1024;  // (kernel, dynamic smem, block, device) entries
 std::atomic<int> g_sms[kMaxDevices];
 struct OccEntry {
     const void *kernel;
