@@ -162,10 +162,10 @@ __device__ __forceinline__ void take_wide_sources(In &in, const LaneSlots<2 * W,
 //   Slots                               a LaneSlots type
 //   issue(const Slots&, c)              the lane's copies of full chunk c
 //   take(In&, const Slots&)             fill In from the stage, as load<false> would
-// A stage is overwritten only STAGES - 1 chunks after it was read, and its reads fed
-// that chunk's results, which were stored before the new copies are issued. The
-// ragged last chunk, if any, takes the global-memory path. kBlock: threads per CTA of
-// the launch.
+// The stage refilled in an iteration is the one the previous iteration read; those reads
+// fed that chunk's results, which were stored before the new copies are issued, so no
+// copy lands in bytes still to be read. The ragged last chunk, if any, takes the
+// global-memory path. kBlock: threads per CTA of the launch.
 template <int STAGES, int kBlock = kThreads, class Op>
 __device__ __forceinline__ void run_chunks_lane_async(const Op &op, int64_t nblk, int chunk_blocks,
                                                       unsigned char *warp_smem)
