@@ -473,7 +473,8 @@ ring_hop_i8_wide_kernel(const int8_t *__restrict__ q_in, const float *__restrict
 // 298 with two, 231 against 243 with one; at 2 CTAs per SM (121 registers for four
 // sources, two 36 KB stages per CTA). Four sources at 3 CTAs per SM took 394 us, with
 // 3 stages 395 us, one CTA of 4 stages 500 us. With the owner output the same loads
-// were 5% slower than direct ones, so that form keeps the direct path.
+// were 5% slower than direct ones (604 against 574 us, in 256- and in 512-thread CTAs),
+// so that form keeps the direct path.
 #ifndef BQ_ACCUM_ASYNC
 #define BQ_ACCUM_ASYNC 1
 #endif
