@@ -143,3 +143,43 @@ def test_end_to_end_pipeline_copies_back_the_device_results():
     for p in ee.sets:  # both buffer sets computed the same step
         for t, w in zip(p.results(), want):
             assert torch.equal(t, w)
+
+
+def test_concurrent_streams_equal_serial():
+    # A call draws only on its arguments and its CTAs' shared memory: the same chain on
+    # four streams at once (separate buffers, the same inputs) gives the bytes of one
+    # serial run, for the async accumulates and reduce as for the other kernels.
+    xs = [x.cuda() for x in inputs.a2a_3072(rows=1024)]
+    n = xs[0].numel()
+
+    def chain():
+        wires = [codec.empty_wire_i8(n) for _ in range(4)]
+        for x, w in zip(xs, wires):
+            codec.quant_i8(x.reshape(-1), w[1], w[2])
+        _, qa, sa = codec.empty_wire_i8(n)
+        codec.dequant_accum_i8([w[1] for w in wires], [w[2] for w in wires], qa, sa, None)
+        out = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        codec.dequant_i8(qa, sa, out)
+        _, qh, sh = codec.empty_wire_i8(n)
+        codec.ring_hop_i8(wires[0][1], wires[0][2], xs[1].reshape(-1), qh, sh, None)
+        _, qr, sr = codec.empty_wire_i8(n)
+        codec.reduce_quant_i8([x.reshape(-1) for x in xs], qr, sr, None)
+        mx = [codec.empty_wire_mx(n) for _ in range(4)]
+        for x, w in zip(xs, mx):
+            codec.quant_mx_flat(x.reshape(-1), w[1], w[2])
+        _, qm, sm = codec.empty_wire_mx(n)
+        codec.dequant_accum_mx([w[1] for w in mx], [w[2] for w in mx], qm, sm, None)
+        return [qa, sa, out, qh, sh, qr, sr, qm, sm]
+
+    ref = chain()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    results = []
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            results.append(chain())
+    torch.cuda.synchronize()
+    for got in results:
+        for a, b in zip(got, ref):
+            assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
