@@ -183,3 +183,49 @@ def test_concurrent_streams_equal_serial():
     for got in results:
         for a, b in zip(got, ref):
             assert torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+
+
+def test_first_call_inside_graph_capture():
+    # A fresh process whose first codec calls happen inside a CUDA-graph capture: the
+    # kernels that raise their shared-memory limit and query occupancy on first use
+    # (async accumulates and reduce, one-CTA-per-SM launches) capture, and the replay
+    # equals an eager run byte for byte.
+    import os
+    import subprocess
+    import sys
+    code = r"""
+import sys, torch
+from block_quantized_wire_gb300 import codec, inputs
+xs = [x.cuda() for x in inputs.a2a_3072(rows=256)]
+n = xs[0].numel()
+def bufs():
+    return [codec.empty_wire_i8(n) for _ in range(4)], codec.empty_wire_i8(n), codec.empty_wire_i8(n), \
+        [codec.empty_wire_mx(n) for _ in range(4)], codec.empty_wire_mx(n)
+def run(b):
+    w, a, r, mw, ma = b
+    for x, wi in zip(xs, w):
+        codec.quant_i8(x.reshape(-1), wi[1], wi[2])
+    codec.dequant_accum_i8([wi[1] for wi in w], [wi[2] for wi in w], a[1], a[2], None)
+    codec.reduce_quant_i8([x.reshape(-1) for x in xs], r[1], r[2], None)
+    for x, wi in zip(xs, mw):
+        codec.quant_mx_flat(x.reshape(-1), wi[1], wi[2])
+    codec.dequant_accum_mx([wi[1] for wi in mw], [wi[2] for wi in mw], ma[1], ma[2], None)
+    return [a[0], r[0], ma[0]]
+side = torch.cuda.Stream()
+side.wait_stream(torch.cuda.current_stream())
+g = torch.cuda.CUDAGraph()
+gb = bufs()
+with torch.cuda.graph(g, stream=side):
+    got = run(gb)
+g.replay()
+torch.cuda.synchronize()
+want = run(bufs())
+torch.cuda.synchronize()
+ok = all(torch.equal(a, b) for a, b in zip(got, want))
+print("equal" if ok else "differ")
+sys.exit(0 if ok else 1)
+"""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, PYTHONPATH=root + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "equal" in r.stdout, r.stdout + r.stderr
