@@ -409,6 +409,28 @@ def test_e4m3_encode_exhaustive_vs_nearest_search():
     assert np.array_equal(got_neg, expect | 0x80)
 
 
+def test_e4m3_encode_matches_torch_float8_e4m3fn():
+    # PyTorch's float8_e4m3fn is an independent implementation of OCP E4M3 (the format
+    # "standard MXFP8" names): its largest finite value is the 448 the scale rules
+    # divide by, and its round-to-nearest-even conversion keeps the sign of zero. Every
+    # BF16 value with |y| <= 464 (beyond 464 PyTorch's conversion gives NaN where a
+    # saturating one gives 448; no scaled MX value gets there), both signs, subnormals
+    # and zeros included, encodes to the same byte.
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("this torch has no float8_e4m3fn")
+    assert float(torch.finfo(f8).max) == 448.0
+    bits = np.arange(0, 0x43E9, dtype=np.uint16)  # 0 .. 464 in BF16
+    ys = _bits_to_f32(bits)
+    for sign in (1.0, -1.0):
+        v = (ys * np.float32(sign)).astype(np.float32)
+        want = torch.from_numpy(v).to(f8).view(torch.uint8).numpy()
+        got = np.array([oracle.e4m3_encode(float(y)) for y in v], np.uint8)
+        bad = np.flatnonzero(got != want)
+        assert bad.size == 0, (sign, [(float(v[i]), int(got[i]), int(want[i])) for i in bad[:5]])
+    assert oracle.e4m3_encode(-0.0) == 0x80 and oracle.e4m3_encode(0.0) == 0x00
+
+
 def test_e4m3_decode_exhaustive():
     for code, v in exact.e4m3_values():
         assert F(oracle.e4m3_decode(code)) == v
