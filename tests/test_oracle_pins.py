@@ -839,6 +839,43 @@ def _torch_block_layout():
     return ns["to_blocked"], ns["from_blocked"]
 
 
+def _torch_to_mxfp():
+    import ast
+    path = os.path.join(os.path.dirname(torch.__file__), "testing", "_internal", "common_quantized.py")
+    if not os.path.exists(path) or not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("this torch build has no MX reference")
+    tree = ast.parse(open(path).read(), path)
+    funcs = [n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name == "to_mxfp"]
+    if not funcs:
+        pytest.skip("torch's common_quantized.py has no to_mxfp")
+    ns = {"torch": torch}
+    exec(compile(ast.Module(body=funcs, type_ignores=[]), path, "exec"), ns)
+    return ns["to_mxfp"]
+
+
+def test_mx_quant_equals_torch_to_mxfp():
+    # PyTorch's MXFP8 reference for its block-scaled GEMM tests (to_mxfp, "RCEIL") states
+    # the same rule independently: E8M0 = ceil(log2(fl(amax/448))) + 127, elements
+    # x * 2^(127 - E8M0) saturated to +-448 and cast to E4M3 with ties to even. Its
+    # readings differ only where this test does not go: an all-zero group gets E8M0 0
+    # there (127 by the pages' rule), and groups with amax/448 below 2^-127 are clamped.
+    # Magnitudes per group span 2^-100 .. 2^100; a BF16 amax is never close enough above
+    # a power of two for its float32 log2 to round to the power itself.
+    to_mxfp = _torch_to_mxfp()
+    rng = np.random.default_rng(61)
+    rows, cols = 96, 2048
+    mag = np.exp2(rng.integers(-100, 101, size=(rows, cols // 32))).repeat(32, axis=1)
+    v = rng.standard_normal((rows, cols)) * mag
+    v[0, :32] = 448.0 * np.exp2(np.arange(32) % 5 - 2)  # amax exactly 448 * 2^k
+    v[1, :32] = np.where(np.arange(32) == 7, 1.0e4, rng.standard_normal(32))  # one outlier
+    xt = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+    xb = xt.view(torch.int16).numpy().view(np.uint16)
+    scale_t, data_t = to_mxfp(xt, 32, "mxfp8")
+    q, sc = oracle.quant_mx(xb)
+    assert np.array_equal(sc, scale_t.view(torch.uint8).numpy())
+    assert np.array_equal(q, data_t.view(torch.uint8).numpy())
+
+
 @pytest.mark.parametrize("rows,g", [(128, 4), (128, 224), (200, 8), (200, 224), (4096, 4), (4096, 224),
                                     (4096, 1344), (257, 1344)])
 def test_mx_tiled_scale_layout_equals_torch_to_blocked(rows, g):
