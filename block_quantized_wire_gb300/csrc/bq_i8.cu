@@ -118,8 +118,15 @@ quant_i8_staged_kernel(const uint16_t *__restrict__ x, int64_t nblk, int8_t *__r
 template <int SEGS>
 using DequantI8 = DequantOp<I8Codec, SEGS>;
 
+// Threads per CTA of the INT8 materialization: 256, 512 and 768 measured the same in the
+// prefill step (225.3 us per launch); 1024 was slower in an A/B (243.9 against 241.5 us).
+#ifndef BQ_DEQUANT_I8_THREADS
+#define BQ_DEQUANT_I8_THREADS 256
+#endif
+constexpr int kDequantI8Threads = BQ_DEQUANT_I8_THREADS;
+
 template <int SEGS>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kDequantI8Threads)
 dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int64_t nblk, uint16_t *__restrict__ out)
 {
     pdl_begin();
@@ -128,7 +135,7 @@ dequant_i8_kernel(const int8_t *__restrict__ q, const float *__restrict__ s, int
     dbg_bf16(out, nblk, true);
     dbg_ready();
     const DequantI8<SEGS> op{q, s, out, nblk, (int)(threadIdx.x & 31)};
-    run_chunks<true>(op, nblk, 2 * SEGS);
+    run_chunks<true, kDequantI8Threads>(op, nblk, 2 * SEGS);
 }
 
 // ---------------------------------------------------------------- accumulate
@@ -777,8 +784,11 @@ cudaError_t read_wait_counters_i8(unsigned long long (&v)[3]) { return read_wait
 
 cudaError_t launch_dequant_i8(const int8_t *q, const float *s, int64_t nblk, uint16_t *out, cudaStream_t st)
 {
-    BQK_GRID(dequant_i8_kernel<kSegsDequant>, chunks(nblk, kSegsDequant));
-    return launch_kernel(dequant_i8_kernel<kSegsDequant>, grid, st, q, s, nblk, out);
+    int grid = 0;
+    if (cudaError_t e = grid_for((const void *)dequant_i8_kernel<kSegsDequant>, chunks(nblk, kSegsDequant), &grid, 0,
+                                 kDequantI8Threads))
+        return e;
+    return launch_kernel_block(dequant_i8_kernel<kSegsDequant>, grid, kDequantI8Threads, 0, st, q, s, nblk, out);
 }
 
 // One source width is compiled per common case (1, 2, 3, 4 sources at once); more
