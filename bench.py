@@ -501,6 +501,46 @@ def oracle_sample(pipe_inputs, rows: int, slice_rows: int, threads: int = 1):
     return time.perf_counter() - t0, nbytes
 
 
+def oracle_next_rows(pipe_inputs, rows: int) -> dict:
+    """The oracle on each of the next rows' operations, single-threaded, on the first `rows`
+    rows of the prefill buffers (W = 4 sources where the row has sources) and of the
+    first MX slice: GB/s of the algorithmic bytes the GPU rows count. Inputs the
+    operation consumes (wires, FP16 copies) are prepared outside its timed call."""
+    import numpy as np
+
+    import oracle
+    from block_quantized_wire_gb300.inputs import bf16_bits
+    xs, slices = pipe_inputs
+    xb = [bf16_bits(x[:rows]).reshape(-1) for x in xs]
+    n = xb[0].size
+    sl_t = slices[0][:rows]
+    sl = bf16_bits(sl_t).reshape(rows, HIDDEN)
+    sl16 = sl_t.to(torch.float16).contiguous().view(torch.int16).numpy().view(np.uint16).reshape(rows, HIDDEN)
+    mx = [oracle.quant_mx_flat(b) for b in xb]
+    e4 = oracle.quant_e4m3(xb[0])
+    _, s_mx = oracle.quant_mx(sl)
+    out = {}
+
+    def timed(name, fn, values):
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        out[name] = {"GB/s": round(kernel_bytes(name, values) / dt / 1e9, 4), "seconds": round(dt, 3)}
+
+    timed("quant_mx_slices", lambda: oracle.quant_mx(sl), rows * HIDDEN)
+    timed("quant_mx_tiled", lambda: oracle.mx_scales_to_tiled(oracle.quant_mx(sl)[1]), rows * HIDDEN)
+    timed("quant_mx_f16", lambda: oracle.quant_mx(sl16, fmt="f16"), rows * HIDDEN)
+    timed("dequant_accum_mx", lambda: oracle.dequant_accum_mx([q for q, _ in mx], [s for _, s in mx],
+                                                               materialize=False), n)
+    timed("ring_hop_mx", lambda: oracle.ring_hop_mx(mx[0][0], mx[0][1], xb[1]), n)
+    timed("reduce_quant_i8", lambda: oracle.reduce_quant_i8(xb), n)
+    timed("reduce_quant_e4m3", lambda: oracle.reduce_quant_e4m3(xb), n)
+    timed("quant_e4m3", lambda: oracle.quant_e4m3(xb[0]), n)
+    timed("dequant_e4m3", lambda: oracle.dequant_e4m3(*e4), n)
+    del s_mx
+    return {"rows": rows, "cores": 1, "kind": "oracle", "ops": out}
+
+
 def oracle_parity(pipe, rows: int, slice_rows: int) -> dict:
     """Part of the CPU-oracle leg: the step's GPU outputs on the first `rows` rows of every
     INT8 buffer and `slice_rows` rows of every MX slice, compared byte for byte with the
@@ -1007,8 +1047,9 @@ def run_bq(args, rank, world, local):
         dt1, nb1 = oracle_sample(ci, r1, sr1, 1)
         dt, nb = oracle_sample(ci, r, sr, T)
         parity = oracle_parity(pipe, min(64, args.rows), min(64, args.slice_rows))
+        nr = oracle_next_rows(ci, min(256, r, sr))
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": UNIT, "cores": T, "kind": "oracle",
-               "parity_sample": parity,
+               "parity_sample": parity, "next_rows": nr,
                "sample": f"one step of the same pipeline on the first {r} of {args.rows} rows of each INT8 buffer "
                          f"and the first {sr} of {args.slice_rows} rows of each MX slice, cut into {T} row ranges "
                          f"run by {T} host threads ({nb} algorithmic bytes, {dt:.2f} s wall)",

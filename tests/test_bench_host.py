@@ -128,3 +128,17 @@ def test_reference_arm_under_torchrun_world2():
 def test_bench_rejects_too_few_warmup_steps():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_oracle_next_rows_times_every_next_row():
+    # the CPU-oracle leg's timing of the next rows: one entry per next-row kernel the GPU
+    # side reports (the tiled FP16 variant shares quant_mx_tiled's oracle), each positive
+    from block_quantized_wire_gb300 import inputs
+    xs = [inputs.prefill_buffer(w, device="cpu", rows=8) for w in range(bench.W_SRC)]
+    sl = inputs.mx_slices_4096(device="cpu", rows=8)
+    r = bench.oracle_next_rows((xs, sl), 8)
+    assert r["rows"] == 8 and r["cores"] == 1 and r["kind"] == "oracle"
+    want = {"quant_mx_slices", "quant_mx_tiled", "quant_mx_f16", "dequant_accum_mx", "ring_hop_mx",
+            "reduce_quant_i8", "reduce_quant_e4m3", "quant_e4m3", "dequant_e4m3"}
+    assert set(r["ops"]) == want
+    assert all(v["GB/s"] > 0 for v in r["ops"].values())
