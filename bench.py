@@ -518,7 +518,6 @@ def oracle_next_rows(pipe_inputs, rows: int) -> dict:
     sl16 = sl_t.to(torch.float16).contiguous().view(torch.int16).numpy().view(np.uint16).reshape(rows, HIDDEN)
     mx = [oracle.quant_mx_flat(b) for b in xb]
     e4 = oracle.quant_e4m3(xb[0])
-    _, s_mx = oracle.quant_mx(sl)
     out = {}
 
     def timed(name, fn, values):
@@ -537,7 +536,6 @@ def oracle_next_rows(pipe_inputs, rows: int) -> dict:
     timed("reduce_quant_e4m3", lambda: oracle.reduce_quant_e4m3(xb), n)
     timed("quant_e4m3", lambda: oracle.quant_e4m3(xb[0]), n)
     timed("dequant_e4m3", lambda: oracle.dequant_e4m3(*e4), n)
-    del s_mx
     return {"rows": rows, "cores": 1, "kind": "oracle", "ops": out}
 
 
