@@ -26,6 +26,14 @@ OBJDIR = os.path.join(PKG, "_build")
 ALT_LIB = os.path.join(PKG, "libbq_alt.so")
 ALT_OBJDIR = os.path.join(PKG, "_build_alt")
 ALT_FLAGS = ["-DBQ_ACCUM_WIDE=0", "-DBQ_QUANT_WIDE=0", "-DBQ_HOP_WIDE=0", "-DBQ_MX_WIDE=0", "-DBQ_WIDE_V8=0"]
+# The same sources with the loading and CTA-size choices that the per-lane async copies
+# and the one-CTA-per-SM launches were measured against: direct loads in the accumulates
+# and the fused reduce, 256-thread CTAs everywhere. Tests build it to keep those paths
+# bit-exact too.
+DIRECT_LIB = os.path.join(PKG, "libbq_direct.so")
+DIRECT_OBJDIR = os.path.join(PKG, "_build_direct")
+DIRECT_FLAGS = ["-DBQ_ACCUM_ASYNC=0", "-DBQ_ACCUM_MX_ASYNC=0", "-DBQ_REDUCE_ASYNC=0", "-DBQ_QUANT_WIDE_THREADS=256",
+                "-DBQ_HOP_WIDE_THREADS=256", "-DBQ_QUANT_E4M3_THREADS=256", "-DBQ_DEQUANT_MX_THREADS=256"]
 # The debug build: every kernel checks each global access against the buffers its
 # arguments describe and counts (instead of performing) an access outside them.
 DEBUG_LIB = os.path.join(PKG, "libbq_debug.so")
@@ -100,6 +108,11 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=(), li
 def build_alt_library(force: bool = False, verbose: bool = False) -> str:
     """Build libbq_alt.so: the sources with ALT_FLAGS."""
     return build_library(force, verbose, ALT_FLAGS, ALT_LIB, ALT_OBJDIR)
+
+
+def build_direct_library(force: bool = False, verbose: bool = False) -> str:
+    """Build libbq_direct.so: the sources with DIRECT_FLAGS."""
+    return build_library(force, verbose, DIRECT_FLAGS, DIRECT_LIB, DIRECT_OBJDIR)
 
 
 def build_debug_library(force: bool = False, verbose: bool = False) -> str:

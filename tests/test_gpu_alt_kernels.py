@@ -6,12 +6,19 @@ loads in the hops. The alternatives (8 values per lane; bulk-copy-staged hops wi
 their bounded mbarrier waits; 16-byte accesses only) remain in the sources as the
 baseline of those measurements. This module builds them into libbq_alt.so and reruns
 the parity tests that reach them through it.
+
+libbq_direct.so holds the other measured alternatives: direct loads instead of the
+per-lane async copies in the accumulates and the fused reduce, and 256-thread CTAs
+instead of one CTA per SM. The multipass and small-size parity tests rerun through it.
 """
 import pytest
 
+import oracle
 from block_quantized_wire_gb300 import _lib, build
 from tests import test_gpu_i8 as t8
+from tests import test_gpu_multipass as tmp
 from tests import test_gpu_mx_wire as tm
+from tests import test_gpu_next_rows as tn
 from tests import test_gpu_properties as tp
 
 pytestmark = pytest.mark.gpu
@@ -61,3 +68,31 @@ def test_alt_staged_hops_leave_no_abandoned_wait(alt):
     with _lib.use_library(alt):
         tp.test_bounded_waits_do_not_run_out_and_can_be_observed()
         tp.test_fused_owner_output_equals_separate_materialization()
+
+
+@pytest.fixture(scope="module")
+def direct(bq_lib):
+    return build.build_direct_library()
+
+
+def test_direct_loads_and_small_ctas(direct):
+    nblk = tmp.multipass_nblk()
+    xs = [tmp.source_bits(900 + i, nblk) for i in range(4)]
+    sources = (nblk, xs, [oracle.quant_i8(x) for x in xs])
+    with _lib.use_library(direct):
+        tmp.test_quant_dequant_multipass(sources)
+        for owner in (False, True):
+            tmp.test_ring_hop_multipass(sources, owner)
+        for W in (1, 4):
+            tmp.test_accumulate_multipass(sources, W, False)
+        for name in ("i8", "e4m3"):
+            tmp.test_reduce_quant_multipass(sources, name, 4, False)
+        tmp.test_e4m3_quant_dequant_multipass(sources)
+        tmp.test_mx_accumulate_multipass(4)
+        for W in (1, 2, 3, 4):
+            for nblk_small in (37, 8, 1):
+                t8.test_accumulate_any_width(W, False, nblk_small)
+                tm.test_mx_accumulate_any_width(W, False, nblk_small)
+        for name in list(tn.CODECS):
+            for nblk_small in (1, 9, 65):
+                tn.test_reduce_quant_ragged(name, nblk_small)
